@@ -1,0 +1,164 @@
+/*
+ * tw.h -- C ABI of libtw.so: TokenWeave's fused reduce + residual add +
+ * RMSNorm, recast for one GB300 (sm_103a) whose HBM holds all N rank partials.
+ *
+ * What it computes, per token t in [t0, t1) and feature h in [0, H):
+ *
+ *   x[t,h]            = (sum_{r=0}^{N-1} partials[r][t,h]) + residual[t,h]
+ *   residual_out[t,h] = x[t,h]                                 rounded to dtype
+ *   rms[t]            = sqrt( (1/H) * sum_h x[t,h]^2 + eps )
+ *   out[k][t,h]       = x[t,h] / rms[t] * weight[h]   for k in [0, n_out), rounded to dtype
+ *
+ * Sources (page title, section):
+ *   "TokenWeave 策略详解：以大模型推理为例", §1 背景: the layer output is
+ *       RMSNorm(residual + allreduce_output) * weight, per token over all H
+ *       features; the AllReduce is the sum of the rank partials.
+ *   same page, §2 核心思想 and §3.2-3.4: the reordered ReduceScatter on token
+ *       boundaries -> residual add -> RMSNorm -> AllGather; here the token
+ *       range [t0, t1) is one rank's slice and the n_out destinations stand in
+ *       for the AllGather buffers.
+ *   same page, §5 融合内核: one launch, the sum taken at load time, residual
+ *       and variance in registers, the result stored straight to the gather
+ *       destinations.
+ *   "TokenWeave: Efficient Compute-Communication Overlap for Distributed LLM
+ *       Inference" (gist.science summary), "Der intelligente Split" and
+ *       "Der Fused Kernel": a two-chunk token split run on two streams, and a
+ *       fused kernel held to a small SM budget.
+ * Readings where the pages are silent: eps inside the square root; no bias and
+ * no (1 + w) offset; fp32 accumulation, the partials summed in rank order and
+ * the residual added after them; the norm uses the fp32 x, not its rounded
+ * copy; rounding to bf16 is round-to-nearest-even.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named partials/out are HOST arrays of DEVICE pointers (read
+ *     during the call only).  Every other data pointer is a DEVICE pointer on
+ *     the current CUDA device.  The caller owns all memory; the library
+ *     allocates no device memory per call.
+ *   - Tensors are dense row-major: partials[r], residual, out[k] and
+ *     residual_out are [T, H] with row stride H elements; weight is [H].  All
+ *     share one dtype (tw_dtype).
+ *   - Only rows [t0, t1) of residual_out and of every out[k] are written; no
+ *     other byte of any buffer is touched.  t0 == t1 returns TW_OK with no
+ *     launch.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  A status other than TW_OK means nothing was launched.
+ *     Faults after launch surface through the stream like any CUDA error.
+ *   - Argument rules, checked on the host before any CUDA call:
+ *       partials/out arrays and every pointer in them non-NULL;
+ *       1 <= n_parts <= TW_MAX_PARTS, 1 <= n_out <= TW_MAX_OUTS;
+ *       T >= 0, 1 <= H <= TW_MAX_H(dtype), 0 <= t0 <= t1 <= T;
+ *       eps finite and >= 0; max_sms >= 1 (values above the SM count clamp);
+ *       H * sizeof(dtype) a multiple of 16 and every pointer 16-byte aligned
+ *       (else TW_ERR_ALIGNMENT);
+ *       residual_out may equal residual exactly (in place); any other overlap
+ *       of an output with an input or with another output is TW_ERR_ALIAS
+ *       (checked on the byte ranges [ptr, ptr + T*H*size)).
+ *   - Errors: the return value is a tw_status; tw_last_error_string() gives a
+ *     message for the calling thread's last failure.
+ *   - Thread safety: calls from several host threads are safe; per-device state
+ *     (SM count, fork/join events) is created once under a lock.
+ */
+#ifndef TW_H
+#define TW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TW_VERSION 10000 /* 1.0.0 */
+
+#define TW_MAX_PARTS 16
+#define TW_MAX_OUTS 8
+/* Largest hidden size: 16384 bf16 or 8192 fp32 features (the row kernel keeps
+ * one token's fp32 x in registers, 64 floats per thread over 256 threads). */
+#define TW_MAX_H_BF16 16384
+#define TW_MAX_H_F32 8192
+
+typedef enum { TW_BF16 = 0, TW_F32 = 1 } tw_dtype;
+
+typedef enum {
+    TW_OK = 0,
+    TW_ERR_INVALID_ARG = -1,
+    TW_ERR_ALIGNMENT = -2,
+    TW_ERR_ALIAS = -3,
+    TW_ERR_CUDA = -4,
+    TW_ERR_UNSUPPORTED = -5
+} tw_status;
+
+/* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
+typedef enum {
+    TW_PATH_AUTO = 0,  /* rows kernel, or warp kernel for decode-size ranges */
+    TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
+                          staged into shared memory by bulk async copies */
+    TW_PATH_WARP = 2   /* one warp per token, no shared memory */
+} tw_path;
+
+/* The fused step on rows [t0, t1), bf16 tensors.  At most max_sms CTAs are
+ * launched, each alone on its SM, so the kernel occupies at most max_sms SMs. */
+int tw_fused_reduce_add_rmsnorm_bf16(const void* const* partials, int n_parts,
+                                     const void* residual, const void* weight,
+                                     void* const* out, int n_out,
+                                     void* residual_out, int64_t T, int64_t H,
+                                     float eps, int64_t t0, int64_t t1,
+                                     int max_sms, void* stream);
+
+/* Same, fp32 tensors. */
+int tw_fused_reduce_add_rmsnorm_f32(const void* const* partials, int n_parts,
+                                    const void* residual, const void* weight,
+                                    void* const* out, int n_out,
+                                    void* residual_out, int64_t T, int64_t H,
+                                    float eps, int64_t t0, int64_t t1,
+                                    int max_sms, void* stream);
+
+/* Same, dtype given as a tw_dtype value. */
+int tw_fused_reduce_add_rmsnorm(const void* const* partials, int n_parts,
+                                const void* residual, const void* weight,
+                                void* const* out, int n_out, void* residual_out,
+                                int64_t T, int64_t H, float eps, int64_t t0,
+                                int64_t t1, int max_sms, void* stream,
+                                int dtype);
+
+/* Same, with the kernel chosen explicitly (tw_path).  smid_log, when not NULL,
+ * is a DEVICE array of at least max_sms uint32 entries; every CTA of the rows
+ * kernel writes the id of the SM it ran on to smid_log[blockIdx.x] (used to
+ * check the SM budget; entries of CTAs not launched are left alone). */
+int tw_fused_reduce_add_rmsnorm_ex(const void* const* partials, int n_parts,
+                                   const void* residual, const void* weight,
+                                   void* const* out, int n_out,
+                                   void* residual_out, int64_t T, int64_t H,
+                                   float eps, int64_t t0, int64_t t1,
+                                   int max_sms, void* stream, int dtype,
+                                   int path, uint32_t* smid_log);
+
+/* Two-chunk token split ("Der intelligente Split"): rows [0, t_split) run on
+ * stream s0 and rows [t_split, T) on stream s1, each a rows-kernel launch with
+ * its own budget of max_sms SMs (so up to 2*max_sms SMs while both run).
+ * t_split < 0 picks T/2.  s1 first waits for work already queued on s0, and
+ * s0 is made to wait for the s1 chunk, so synchronising s0 alone covers both
+ * chunks.  Same argument rules as above, with t_split <= T. */
+int tw_split_launch(const void* const* partials, int n_parts,
+                    const void* residual, const void* weight, void* const* out,
+                    int n_out, void* residual_out, int64_t T, int64_t H,
+                    float eps, int64_t t_split, int max_sms, void* s0, void* s1,
+                    int dtype);
+
+/* Device-side status of the calling thread's current device: nonzero when a
+ * kernel gave up on a bounded wait (an async copy that never completed) since
+ * the last clear.  Reading synchronises nothing; call it after the stream has
+ * finished.  clear != 0 resets the word.  Returns -1 on a CUDA error. */
+int tw_device_status(int clear);
+
+/* Message for the calling thread's last failed call ("" if none). Never NULL. */
+const char* tw_last_error_string(void);
+
+/* TW_VERSION of the loaded library. */
+int tw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TW_H */

@@ -1,0 +1,338 @@
+// tw_api.cu -- the C ABI of libtw.so: argument checks, per-device state,
+// kernel choice and the two-stream token split.  Every rule stated in tw.h is
+// checked here on the host before the first CUDA call of an entry point.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "tw.h"
+#include "tw_internal.h"
+
+namespace tw {
+namespace {
+
+// Bounded-wait give-ups of any kernel on this device (see tw_device_status).
+__device__ unsigned int g_status_word;
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(TW_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Under TW_PATH_AUTO, token ranges of at most this many tokens (decode-size
+// batches) go to the warp kernel, larger ones to the rows kernel.
+constexpr int64_t kWarpPathMaxTokens = 32;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    unsigned int* status = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join = nullptr;
+    std::mutex split_mu;  // orders the record/wait pairs of concurrent splits
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_init_mu;
+DeviceState g_devices[kMaxDevices];
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(TW_ERR_UNSUPPORTED, "device %d", dev);
+    DeviceState& d = g_devices[dev];
+    std::lock_guard<std::mutex> lock(g_init_mu);
+    if (!d.ready) {
+        int major = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major < 10)
+            return fail(TW_ERR_UNSUPPORTED, "device %d has compute capability %d.x; "
+                        "libtw.so is built for sm_103a", dev, major);
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (d.smem_optin < kExclusiveSmemBytes)
+            return fail(TW_ERR_UNSUPPORTED, "device %d allows only %d bytes of shared memory",
+                        dev, d.smem_optin);
+        if ((e = static_cast<cudaError_t>(rows_set_smem_limit(d.smem_optin))) != cudaSuccess ||
+            (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress");
+        if ((e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+        d.ready = true;
+    }
+    *out = &d;
+    return TW_OK;
+}
+
+struct Args {
+    const void* const* partials;
+    int n_parts;
+    const void* residual;
+    const void* weight;
+    void* const* out;
+    int n_out;
+    void* residual_out;
+    int64_t T, H;
+    float eps;
+    int64_t t0, t1;
+    int max_sms;
+    int dtype;
+};
+
+size_t elem_size(int dtype) { return dtype == TW_BF16 ? 2 : 4; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return na != 0 && nb != 0 && a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// All host-side rules of tw.h; no CUDA call.
+int check_args(const Args& a) {
+    if (a.dtype != TW_BF16 && a.dtype != TW_F32)
+        return fail(TW_ERR_INVALID_ARG, "dtype %d is not TW_BF16 or TW_F32", a.dtype);
+    if (!a.partials || !a.out || !a.residual || !a.weight || !a.residual_out)
+        return fail(TW_ERR_INVALID_ARG, "NULL pointer argument");
+    if (a.n_parts < 1 || a.n_parts > TW_MAX_PARTS)
+        return fail(TW_ERR_INVALID_ARG, "n_parts %d outside [1, %d]", a.n_parts, TW_MAX_PARTS);
+    if (a.n_out < 1 || a.n_out > TW_MAX_OUTS)
+        return fail(TW_ERR_INVALID_ARG, "n_out %d outside [1, %d]", a.n_out, TW_MAX_OUTS);
+    for (int r = 0; r < a.n_parts; ++r)
+        if (!a.partials[r]) return fail(TW_ERR_INVALID_ARG, "partials[%d] is NULL", r);
+    for (int k = 0; k < a.n_out; ++k)
+        if (!a.out[k]) return fail(TW_ERR_INVALID_ARG, "out[%d] is NULL", k);
+    const int64_t max_h = a.dtype == TW_BF16 ? TW_MAX_H_BF16 : TW_MAX_H_F32;
+    if (a.T < 0 || a.H < 1)
+        return fail(TW_ERR_INVALID_ARG, "T %lld and H %lld must satisfy T >= 0, H >= 1",
+                    (long long)a.T, (long long)a.H);
+    if (a.H > max_h)
+        return fail(TW_ERR_UNSUPPORTED, "H %lld above the limit %lld for this dtype",
+                    (long long)a.H, (long long)max_h);
+    if (a.t0 < 0 || a.t0 > a.t1 || a.t1 > a.T)
+        return fail(TW_ERR_INVALID_ARG, "token range [%lld, %lld) not within [0, %lld]",
+                    (long long)a.t0, (long long)a.t1, (long long)a.T);
+    if (!(a.eps >= 0.f) || std::isinf(a.eps))
+        return fail(TW_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (a.max_sms < 1) return fail(TW_ERR_INVALID_ARG, "max_sms %d < 1", a.max_sms);
+
+    const size_t es = elem_size(a.dtype);
+    if ((static_cast<size_t>(a.H) * es) % 16 != 0)
+        return fail(TW_ERR_ALIGNMENT, "H * element size (%lld bytes) is not a multiple of 16",
+                    (long long)(a.H * static_cast<int64_t>(es)));
+    if (misaligned(a.residual) || misaligned(a.weight) || misaligned(a.residual_out))
+        return fail(TW_ERR_ALIGNMENT, "residual, weight and residual_out must be 16-byte aligned");
+    for (int r = 0; r < a.n_parts; ++r)
+        if (misaligned(a.partials[r]))
+            return fail(TW_ERR_ALIGNMENT, "partials[%d] is not 16-byte aligned", r);
+    for (int k = 0; k < a.n_out; ++k)
+        if (misaligned(a.out[k])) return fail(TW_ERR_ALIGNMENT, "out[%d] is not 16-byte aligned", k);
+
+    // Aliasing: outputs against inputs and against each other.
+    const size_t tb = static_cast<size_t>(a.T) * static_cast<size_t>(a.H) * es;
+    const size_t wb = static_cast<size_t>(a.H) * es;
+    const int n_outputs = a.n_out + 1;
+    for (int i = 0; i < n_outputs; ++i) {
+        const void* o = i < a.n_out ? a.out[i] : a.residual_out;
+        const bool is_res_out = i == a.n_out;
+        for (int r = 0; r < a.n_parts; ++r)
+            if (overlaps(o, tb, a.partials[r], tb))
+                return fail(TW_ERR_ALIAS, "an output overlaps partials[%d]", r);
+        if (overlaps(o, tb, a.weight, wb)) return fail(TW_ERR_ALIAS, "an output overlaps weight");
+        if (overlaps(o, tb, a.residual, tb) && !(is_res_out && o == a.residual))
+            return fail(TW_ERR_ALIAS, "an output overlaps residual (only residual_out == "
+                        "residual, exactly, is allowed)");
+        for (int j = i + 1; j < n_outputs; ++j) {
+            const void* o2 = j < a.n_out ? a.out[j] : a.residual_out;
+            if (overlaps(o, tb, o2, tb)) return fail(TW_ERR_ALIAS, "two outputs overlap");
+        }
+    }
+    return TW_OK;
+}
+
+Params make_params(const Args& a, const DeviceState& d, int64_t t0, int64_t t1,
+                   uint32_t* smid_log) {
+    Params p{};
+    for (int r = 0; r < a.n_parts; ++r) p.partials[r] = a.partials[r];
+    for (int k = 0; k < a.n_out; ++k) p.out[k] = a.out[k];
+    p.residual = a.residual;
+    p.weight = a.weight;
+    p.residual_out = a.residual_out;
+    p.smid_log = smid_log;
+    p.status = d.status;
+    p.t0 = t0;
+    p.t1 = t1;
+    p.H = a.H;
+    p.row_bytes = a.H * static_cast<int64_t>(elem_size(a.dtype));
+    p.n_parts = a.n_parts;
+    p.n_out = a.n_out;
+    p.n_chunks = static_cast<int>((p.row_bytes + kChunkBytes - 1) / kChunkBytes);
+    p.eps = a.eps;
+    p.inv_H = static_cast<float>(1.0 / static_cast<double>(a.H));
+    return p;
+}
+
+// Launch one kernel over rows [t0, t1) (non-empty) on `stream`.
+int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, int path,
+                 uint32_t* smid_log, void* stream) {
+    const int64_t tokens = t1 - t0;
+    const int64_t sms = a.max_sms < d.sm_count ? a.max_sms : d.sm_count;
+    Params p = make_params(a, d, t0, t1, smid_log);
+    if (path == TW_PATH_AUTO) path = tokens <= kWarpPathMaxTokens ? TW_PATH_WARP : TW_PATH_ROWS;
+
+    int err;
+    if (path == TW_PATH_ROWS) {
+        const size_t stage = static_cast<size_t>(a.n_parts + 1) * kChunkBytes;
+        int stages = static_cast<int>((static_cast<size_t>(d.smem_optin) - rows_smem_bytes(a.n_parts, 0)) / stage);
+        if (stages > kMaxStages) stages = kMaxStages;
+        if (stages < kMinStages)
+            return fail(TW_ERR_UNSUPPORTED, "shared memory too small for %d partials", a.n_parts);
+        p.stages = stages;
+        size_t smem = rows_smem_bytes(a.n_parts, stages);
+        if (smem < static_cast<size_t>(kExclusiveSmemBytes)) smem = kExclusiveSmemBytes;
+        const int grid = static_cast<int>(tokens < sms ? tokens : sms);
+        err = launch_rows(p, a.dtype, grid, smem, stream);
+    } else if (path == TW_PATH_WARP) {
+        const int64_t ctas = (tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta;
+        const int grid = static_cast<int>(ctas < sms ? ctas : sms);
+        err = launch_warp(p, a.dtype, grid, kExclusiveSmemBytes, stream);
+    } else {
+        return fail(TW_ERR_INVALID_ARG, "unknown path %d", path);
+    }
+    if (err != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(err), "kernel launch");
+    return TW_OK;
+}
+
+int fused(const Args& a, int path, uint32_t* smid_log, void* stream) {
+    int rc = check_args(a);
+    if (rc != TW_OK) return rc;
+    if (path < TW_PATH_AUTO || path > TW_PATH_WARP)
+        return fail(TW_ERR_INVALID_ARG, "unknown path %d", path);
+    if (a.t0 == a.t1) return TW_OK;
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != TW_OK) return rc;
+    return launch_range(a, *d, a.t0, a.t1, path, smid_log, stream);
+}
+
+}  // namespace
+}  // namespace tw
+
+using tw::Args;
+
+extern "C" {
+
+int tw_fused_reduce_add_rmsnorm_ex(const void* const* partials, int n_parts,
+                                   const void* residual, const void* weight,
+                                   void* const* out, int n_out, void* residual_out, int64_t T,
+                                   int64_t H, float eps, int64_t t0, int64_t t1, int max_sms,
+                                   void* stream, int dtype, int path, uint32_t* smid_log) {
+    const Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+                 T,        H,       eps,      t0,     t1,  max_sms, dtype};
+    return tw::fused(a, path, smid_log, stream);
+}
+
+int tw_fused_reduce_add_rmsnorm(const void* const* partials, int n_parts, const void* residual,
+                                const void* weight, void* const* out, int n_out,
+                                void* residual_out, int64_t T, int64_t H, float eps, int64_t t0,
+                                int64_t t1, int max_sms, void* stream, int dtype) {
+    return tw_fused_reduce_add_rmsnorm_ex(partials, n_parts, residual, weight, out, n_out,
+                                          residual_out, T, H, eps, t0, t1, max_sms, stream,
+                                          dtype, TW_PATH_AUTO, nullptr);
+}
+
+int tw_fused_reduce_add_rmsnorm_bf16(const void* const* partials, int n_parts,
+                                     const void* residual, const void* weight,
+                                     void* const* out, int n_out, void* residual_out,
+                                     int64_t T, int64_t H, float eps, int64_t t0, int64_t t1,
+                                     int max_sms, void* stream) {
+    return tw_fused_reduce_add_rmsnorm(partials, n_parts, residual, weight, out, n_out,
+                                       residual_out, T, H, eps, t0, t1, max_sms, stream,
+                                       TW_BF16);
+}
+
+int tw_fused_reduce_add_rmsnorm_f32(const void* const* partials, int n_parts,
+                                    const void* residual, const void* weight, void* const* out,
+                                    int n_out, void* residual_out, int64_t T, int64_t H,
+                                    float eps, int64_t t0, int64_t t1, int max_sms,
+                                    void* stream) {
+    return tw_fused_reduce_add_rmsnorm(partials, n_parts, residual, weight, out, n_out,
+                                       residual_out, T, H, eps, t0, t1, max_sms, stream, TW_F32);
+}
+
+int tw_split_launch(const void* const* partials, int n_parts, const void* residual,
+                    const void* weight, void* const* out, int n_out, void* residual_out,
+                    int64_t T, int64_t H, float eps, int64_t t_split, int max_sms, void* s0,
+                    void* s1, int dtype) {
+    const Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+                 T,        H,       eps,      0,      T,   max_sms, dtype};
+    int rc = tw::check_args(a);
+    if (rc != TW_OK) return rc;
+    if (t_split < 0) t_split = T / 2;
+    if (t_split > T)
+        return tw::fail(TW_ERR_INVALID_ARG, "t_split %lld > T %lld", (long long)t_split,
+                        (long long)T);
+    if (T == 0) return TW_OK;
+    tw::DeviceState* d = nullptr;
+    if ((rc = tw::device_state(&d)) != TW_OK) return rc;
+
+    cudaStream_t st0 = static_cast<cudaStream_t>(s0), st1 = static_cast<cudaStream_t>(s1);
+    std::lock_guard<std::mutex> lock(d->split_mu);
+    cudaError_t e;
+    if ((e = cudaEventRecord(d->fork, st0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st1, d->fork, 0)) != cudaSuccess)
+        return tw::cuda_fail(e, "fork");
+    if (t_split > 0 &&
+        (rc = tw::launch_range(a, *d, 0, t_split, TW_PATH_ROWS, nullptr, s0)) != TW_OK)
+        return rc;
+    if (t_split < T &&
+        (rc = tw::launch_range(a, *d, t_split, T, TW_PATH_ROWS, nullptr, s1)) != TW_OK)
+        return rc;
+    if ((e = cudaEventRecord(d->join, st1)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st0, d->join, 0)) != cudaSuccess)
+        return tw::cuda_fail(e, "join");
+    return TW_OK;
+}
+
+int tw_device_status(int clear) {
+    unsigned int word = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&word, tw::g_status_word, sizeof(word));
+    if (e != cudaSuccess) return tw::cuda_fail(e, "cudaMemcpyFromSymbol"), -1;
+    if (clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(tw::g_status_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return tw::cuda_fail(e, "cudaMemcpyToSymbol"), -1;
+    }
+    return static_cast<int>(word);
+}
+
+const char* tw_last_error_string(void) { return tw::t_last_error.c_str(); }
+
+int tw_version(void) { return TW_VERSION; }
+
+}  // extern "C"

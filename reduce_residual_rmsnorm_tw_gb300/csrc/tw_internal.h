@@ -1,0 +1,54 @@
+// tw_internal.h -- launch parameters shared by the host API and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+#include "tw.h"
+
+namespace tw {
+
+// Consumer threads of the rows kernel: one 16-byte vector per thread per
+// staged chunk, so a chunk row is kRowsThreads * 16 bytes.
+constexpr int kRowsThreads = 256;
+constexpr int kChunkBytes = kRowsThreads * 16;
+// Chunks per token the rows kernel keeps in registers (H <= 8 * 4 KB bytes).
+constexpr int kMaxChunks = 8;
+// Ring depth bounds of the rows kernel.
+constexpr int kMaxStages = 16;
+constexpr int kMinStages = 2;
+// Dynamic shared memory every rows/warp CTA asks for at least: above half of
+// an SM's 228 KB, so no two CTAs of a launch share an SM and a grid of at most
+// max_sms CTAs occupies at most max_sms SMs.
+constexpr int kExclusiveSmemBytes = 120 * 1024;
+// Warps per CTA of the warp-per-token kernel.
+constexpr int kWarpTokensPerCta = 4;
+
+struct Params {
+    const void* partials[TW_MAX_PARTS];
+    void* out[TW_MAX_OUTS];
+    const void* residual;
+    const void* weight;
+    void* residual_out;
+    uint32_t* smid_log;     // optional, rows kernel only
+    unsigned int* status;   // device status word (bounded-wait give-ups)
+    int64_t t0, t1;         // token range
+    int64_t row_bytes;      // H * element size (multiple of 16)
+    int64_t H;
+    int n_parts, n_out;
+    int n_chunks;           // ceil(row_bytes / kChunkBytes), rows kernel
+    int stages;             // ring depth, rows kernel
+    float eps;
+    float inv_H;
+};
+
+// Launchers (return a cudaError_t value as int).
+int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, void* stream);
+int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, void* stream);
+// Shared memory the rows kernel needs for a given ring depth.
+size_t rows_smem_bytes(int n_parts, int stages);
+// Raise the dynamic shared memory limit of every kernel instantiation on the
+// current device (cudaError_t as int).
+int rows_set_smem_limit(int smem_optin);
+int warp_set_smem_limit(int smem_optin);
+
+}  // namespace tw

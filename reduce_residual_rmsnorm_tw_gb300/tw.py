@@ -1,0 +1,193 @@
+"""Thin ctypes binding of libtw.so (argument marshalling only).
+
+Every function keeps the name of the C entry point it calls.  Tensors are
+torch tensors used only as device memory: the binding reads their pointers,
+shapes and dtypes, the library checks the rules of ``include/tw.h`` and runs
+every step of the computation in its CUDA kernels.  There is no fallback: if
+``libtw.so`` is missing the first call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtw.so")
+
+TW_BF16, TW_F32 = 0, 1
+PATHS = {"auto": 0, "rows": 1, "warp": 2}
+MAX_PARTS, MAX_OUTS = 16, 8
+STATUS_NAMES = {0: "TW_OK", -1: "TW_ERR_INVALID_ARG", -2: "TW_ERR_ALIGNMENT",
+                -3: "TW_ERR_ALIAS", -4: "TW_ERR_CUDA", -5: "TW_ERR_UNSUPPORTED"}
+_DTYPES = {torch.bfloat16: TW_BF16, torch.float32: TW_F32}
+_ALL_SMS = 1 << 30  # clamped to the device's SM count by the library
+
+
+class TwError(RuntimeError):
+    """A libtw.so call returned a status other than TW_OK."""
+
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load():
+    """Load libtw.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    common = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64,
+              ctypes.c_float, i64, i64, ctypes.c_int, vp]
+    for name, extra in (("tw_fused_reduce_add_rmsnorm_bf16", []),
+                        ("tw_fused_reduce_add_rmsnorm_f32", []),
+                        ("tw_fused_reduce_add_rmsnorm", [ctypes.c_int]),
+                        ("tw_fused_reduce_add_rmsnorm_ex",
+                         [ctypes.c_int, ctypes.c_int, vp])):
+        fn = getattr(lib, name)
+        fn.argtypes = common + extra
+        fn.restype = ctypes.c_int
+    lib.tw_split_launch.argtypes = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int,
+                                    vp, i64, i64, ctypes.c_float, i64,
+                                    ctypes.c_int, vp, vp, ctypes.c_int]
+    lib.tw_split_launch.restype = ctypes.c_int
+    lib.tw_device_status.argtypes = [ctypes.c_int]
+    lib.tw_device_status.restype = ctypes.c_int
+    lib.tw_last_error_string.argtypes = []
+    lib.tw_last_error_string.restype = ctypes.c_char_p
+    lib.tw_version.argtypes = []
+    lib.tw_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc != 0:
+        raise TwError(rc, load().tw_last_error_string().decode())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _marshal(partials, residual, weight, out, residual_out):
+    """Pointer arrays and (T, H, dtype) from tensors; shapes must agree."""
+    partials, out = list(partials), list(out)
+    if not partials or not out:
+        raise ValueError("need at least one partial and one destination")
+    if residual.dim() != 2:
+        raise ValueError("residual must be [T, H]")
+    T, H = residual.shape
+    dtype = residual.dtype
+    if dtype not in _DTYPES:
+        raise ValueError(f"dtype {dtype} not supported (bfloat16 or float32)")
+    for name, ts in (("partials", partials), ("out", out),
+                     ("residual_out", [residual_out])):
+        for t in ts:
+            if t.shape != (T, H) or t.dtype != dtype or not t.is_contiguous():
+                raise ValueError(f"{name}: every tensor must be a contiguous "
+                                 f"[{T}, {H}] {dtype} tensor")
+    if (weight.shape != (H,) or weight.dtype != dtype
+            or not weight.is_contiguous()):
+        raise ValueError(f"weight must be a contiguous [{H}] {dtype} tensor")
+    p_arr = (ctypes.c_void_p * len(partials))(*[t.data_ptr() for t in partials])
+    o_arr = (ctypes.c_void_p * len(out))(*[t.data_ptr() for t in out])
+    return p_arr, len(partials), o_arr, len(out), T, H, _DTYPES[dtype]
+
+
+def tw_fused_reduce_add_rmsnorm_ex(partials, residual, weight, out,
+                                   residual_out, eps, t0=0, t1=None,
+                                   max_sms=None, stream=None, path="auto",
+                                   smid_log=None):
+    """Fused reduce + residual add + RMSNorm on rows [t0, t1), kernel chosen
+    by ``path`` ("auto", "rows" or "warp").  ``smid_log`` is an optional int32
+    device tensor with at least max_sms entries."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    rc = load().tw_fused_reduce_add_rmsnorm_ex(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+        _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt,
+        PATHS[path], None if smid_log is None else smid_log.data_ptr())
+    _check(rc)
+
+
+def tw_fused_reduce_add_rmsnorm(partials, residual, weight, out, residual_out,
+                                eps, t0=0, t1=None, max_sms=None, stream=None):
+    """Fused reduce + residual add + RMSNorm on rows [t0, t1) (kernel chosen
+    by the library)."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    rc = load().tw_fused_reduce_add_rmsnorm(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+        _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt)
+    _check(rc)
+
+
+def _typed(name, dtype):
+    def call(partials, residual, weight, out, residual_out, eps, t0=0, t1=None,
+             max_sms=None, stream=None):
+        if residual.dtype != dtype:
+            raise ValueError(f"{name} takes {dtype} tensors")
+        p_arr, n, o_arr, n_out, T, H, _ = _marshal(partials, residual, weight,
+                                                   out, residual_out)
+        rc = getattr(load(), name)(
+            p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+            residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+            _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream))
+        _check(rc)
+    call.__name__ = name
+    call.__doc__ = f"The fused step on {dtype} tensors (C entry point {name})."
+    return call
+
+
+tw_fused_reduce_add_rmsnorm_bf16 = _typed("tw_fused_reduce_add_rmsnorm_bf16",
+                                          torch.bfloat16)
+tw_fused_reduce_add_rmsnorm_f32 = _typed("tw_fused_reduce_add_rmsnorm_f32",
+                                         torch.float32)
+
+
+def tw_split_launch(partials, residual, weight, out, residual_out, eps,
+                    t_split=-1, max_sms=None, s0=None, s1=None):
+    """Two-chunk token split: rows [0, t_split) on s0, [t_split, T) on s1.
+    Synchronising s0 covers both chunks."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    if s1 is None:
+        raise ValueError("tw_split_launch needs a second stream s1")
+    rc = load().tw_split_launch(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t_split,
+        _ALL_SMS if max_sms is None else max_sms, _stream_handle(s0),
+        _stream_handle(s1), dt)
+    _check(rc)
+
+
+def tw_device_status(clear=False):
+    """Device status word: nonzero if a kernel gave up on a bounded wait."""
+    rc = load().tw_device_status(1 if clear else 0)
+    if rc < 0:
+        raise TwError(-4, load().tw_last_error_string().decode())
+    return rc
+
+
+def tw_last_error_string():
+    return load().tw_last_error_string().decode()
+
+
+def tw_version():
+    return load().tw_version()

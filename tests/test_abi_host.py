@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every function include/tw.h declares, and refuses bad arguments with the
+documented status before any CUDA call.  Only fake (never dereferenced)
+addresses are passed, and every call here returns before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from reduce_residual_rmsnorm_tw_gb300 import build as twbuild
+from reduce_residual_rmsnorm_tw_gb300 import tw
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "tw.h")
+
+OK, INVALID, ALIGN, ALIAS, CUDA, UNSUP = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    twbuild.build()
+    return tw.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tw_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8, names
+    for name in names:
+        assert hasattr(lib, name), f"libtw.so does not export {name}"
+
+
+def test_version_and_error_string(lib):
+    assert tw.tw_version() == 10000
+    assert isinstance(tw.tw_last_error_string(), str)
+
+
+BASE = 0x7f0000000000  # fake, 16-byte aligned device addresses (never used)
+MB = 1 << 20
+
+
+def call(lib, n_parts=2, n_out=1, T=4, H=64, eps=1e-6, t0=0, t1=None,
+         max_sms=8, dtype=0, path=0, partials=None, out=None, residual=None,
+         weight=None, residual_out=None):
+    t1 = T if t1 is None else t1
+    partials = partials if partials is not None else [BASE + i * MB for i in range(n_parts)]
+    out = out if out is not None else [BASE + (32 + k) * MB for k in range(n_out)]
+    residual = BASE + 64 * MB if residual is None else residual
+    weight = BASE + 65 * MB if weight is None else weight
+    residual_out = BASE + 66 * MB if residual_out is None else residual_out
+    p_arr = (ctypes.c_void_p * max(1, len(partials)))(*partials)
+    o_arr = (ctypes.c_void_p * max(1, len(out)))(*out)
+    return lib.tw_fused_reduce_add_rmsnorm_ex(
+        p_arr, n_parts, residual, weight, o_arr, n_out, residual_out, T, H,
+        eps, t0, t1, max_sms, None, dtype, path, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    ({"n_parts": 0}, INVALID),
+    ({"n_parts": 17}, INVALID),
+    ({"n_out": 0}, INVALID),
+    ({"n_out": 9}, INVALID),
+    ({"T": -1, "t1": 0}, INVALID),
+    ({"H": 0}, INVALID),
+    ({"t0": 3, "t1": 2}, INVALID),
+    ({"t1": 5}, INVALID),
+    ({"t0": -1}, INVALID),
+    ({"eps": -1e-6}, INVALID),
+    ({"eps": float("inf")}, INVALID),
+    ({"eps": float("nan")}, INVALID),
+    ({"max_sms": 0}, INVALID),
+    ({"dtype": 2}, INVALID),
+    ({"path": 7}, INVALID),
+    ({"H": 12}, ALIGN),                       # 24 bytes per row
+    ({"H": 6, "dtype": 1}, ALIGN),            # 24 bytes per row
+    ({"residual": BASE + 64 * MB + 8}, ALIGN),
+    ({"partials": [BASE, BASE + MB + 4]}, ALIGN),
+    ({"H": 16392}, UNSUP),                    # above the bf16 limit
+    ({"H": 8196, "dtype": 1}, UNSUP),         # above the fp32 limit
+    ({"residual_out": BASE + 64 * MB + 16}, ALIAS),   # overlaps residual, not equal
+    ({"out": [BASE]}, ALIAS),                          # output == partials[0]
+    ({"out": [BASE + 65 * MB - 64]}, ALIAS),           # overlaps weight
+    ({"n_out": 2, "out": [BASE + 32 * MB, BASE + 32 * MB + 256]}, ALIAS),
+    ({"out": [BASE + 66 * MB]}, ALIAS),                # out == residual_out
+    ({"out": [BASE + 64 * MB]}, ALIAS),                # out == residual
+])
+def test_bad_arguments_are_refused(lib, kwargs, status):
+    assert call(lib, **kwargs) == status
+    assert tw.tw_last_error_string() != ""
+
+
+def test_null_pointers_are_refused(lib):
+    assert call(lib, partials=[BASE, 0]) == INVALID
+    assert call(lib, out=[0]) == INVALID
+    assert call(lib, residual=0) == INVALID
+    p_arr = (ctypes.c_void_p * 1)(BASE)
+    assert lib.tw_fused_reduce_add_rmsnorm_ex(
+        None, 1, BASE + 64 * MB, BASE + 65 * MB, p_arr, 1, BASE + 66 * MB, 4, 64,
+        1e-6, 0, 4, 8, None, 0, 0, None) == INVALID
+
+
+def test_empty_range_is_a_no_op(lib):
+    # t0 == t1 returns TW_OK before any CUDA call, even without a GPU.
+    assert call(lib, t0=2, t1=2) == OK
+    assert call(lib, T=0, t0=0, t1=0) == OK
+
+
+def test_in_place_residual_is_allowed_by_the_checks(lib):
+    # residual_out == residual passes the alias rule; with an empty range no
+    # kernel is launched.
+    assert call(lib, residual_out=BASE + 64 * MB, t0=1, t1=1) == OK
+
+
+def test_split_launch_argument_checks(lib):
+    p_arr = (ctypes.c_void_p * 2)(BASE, BASE + MB)
+    o_arr = (ctypes.c_void_p * 1)(BASE + 32 * MB)
+    args = [p_arr, 2, BASE + 64 * MB, BASE + 65 * MB, o_arr, 1, BASE + 66 * MB]
+    assert lib.tw_split_launch(*args, 8, 64, 1e-6, 9, 8, None, None, 0) == INVALID
+    assert lib.tw_split_launch(*args, 8, 12, 1e-6, 4, 8, None, None, 0) == ALIGN
+    assert lib.tw_split_launch(*args, 0, 64, 1e-6, -1, 8, None, None, 0) == OK
+
+
+def test_binding_marshalling_checks():
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        tw.tw_fused_reduce_add_rmsnorm([x], x, torch.zeros(63, dtype=torch.bfloat16),
+                                       [x.clone()], x.clone(), 1e-6)
+    with pytest.raises(ValueError):
+        tw.tw_fused_reduce_add_rmsnorm([x.float()], x, torch.zeros(64, dtype=torch.bfloat16),
+                                       [x.clone()], x.clone(), 1e-6)
+    with pytest.raises(ValueError):
+        tw.tw_fused_reduce_add_rmsnorm_f32([x], x, torch.zeros(64, dtype=torch.bfloat16),
+                                           [x.clone()], x.clone(), 1e-6)

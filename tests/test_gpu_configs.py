@@ -1,0 +1,61 @@
+"""The five benchmark workloads at full size, in the launch configuration the
+benchmark times, against the oracle: element by element where the oracle
+finishes in seconds (the N=2 and N=8 x 1024-token cases and the decode sweep),
+on sampled tokens otherwise (the 16384-token split and the fp32 column-split
+case, whose inputs are drawn on the device)."""
+import pytest
+import torch
+
+from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+from tests.parity import alloc_outputs, check_sampled, check_workload, sample_tokens
+
+pytestmark = pytest.mark.gpu
+W = inputs.WORKLOADS
+
+
+def test_tp2_t2048_h4096_bf16_full():
+    check_workload(W["tp2_t2048_h4096_bf16"])
+
+
+def test_tp8_t1024_h8192_bf16_full():
+    check_workload(W["tp8_t1024_h8192_bf16"])
+
+
+@pytest.mark.parametrize("max_sms", [2, 8, 148])
+def test_tp8_t1024_h8192_bf16_sm_budgets(max_sms):
+    check_workload(W["tp8_t1024_h8192_bf16"], max_sms=max_sms)
+
+
+@pytest.mark.parametrize("T", inputs.DECODE_TOKENS)
+@pytest.mark.parametrize("path", ["warp", "auto"])
+def test_decode_sweep_full(T, path):
+    check_workload(W["decode_tp8_h8192_bf16"].with_tokens(T), path=path)
+
+
+@pytest.mark.parametrize("max_sms", [8, 148])
+def test_split_t16384_sampled(max_sms):
+    wl = W["split_tp8_t16384_h8192_bf16"]
+    d = inputs.make_inputs(wl, device="cuda")
+    out, res_out = alloc_outputs(wl)
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    tw.tw_split_launch(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps,
+                       t_split=-1, max_sms=max_sms, s0=s0, s1=s1)
+    s0.synchronize()
+    toks = sample_tokens(wl.T, 96, seed=3, must=(0, 1, 8191, 8192, 8193, wl.T - 1))
+    check_sampled(wl, d, out, res_out, toks)
+    assert bool(torch.isfinite(out[0].float()).all())
+    assert bool(torch.isfinite(res_out.float()).all())
+
+
+def test_colsplit_t8192_h5120_f32_sampled():
+    wl = W["colsplit_tp4_t8192_h5120_f32_out4"]
+    d = inputs.make_inputs(wl, device="cuda")
+    out, res_out = alloc_outputs(wl)
+    tw.tw_fused_reduce_add_rmsnorm(d["partials"], d["residual"], d["weight"], out, res_out,
+                                   wl.eps)
+    torch.cuda.synchronize()
+    toks = sample_tokens(wl.T, 128, seed=4, must=(0, wl.T - 1))
+    check_sampled(wl, d, out, res_out, toks)
+    for k in range(1, wl.n_out):
+        assert torch.equal(out[k], out[0])
+    assert bool(torch.isfinite(out[0]).all()) and bool(torch.isfinite(res_out).all())

@@ -1,0 +1,81 @@
+"""CUDA path vs the fp64 oracle, element by element, at sizes the oracle
+finishes in seconds: several chunks and CTAs per launch, ragged chunk tails,
+sub-ranges, in-place residual, several destinations, both dtypes, both
+kernels, and the edge cases (empty range, one token, maximum H and N)."""
+import pytest
+import torch
+
+from reduce_residual_rmsnorm_tw_gb300.inputs import Workload
+from tests.parity import check_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(n, T, H, dtype="bf16", n_out=1, eps=1e-6, seed=11, column=False, std=1.0):
+    return Workload(f"n{n}_t{T}_h{H}_{dtype}_o{n_out}", n, T, H, dtype, eps, n_out, seed,
+                    partial_std=std, column_split=column)
+
+
+CASES = [
+    wl(1, 5, 8),                       # one 16-byte vector per row
+    wl(2, 37, 4096),                   # two full chunks per token
+    wl(3, 50, 1000),                   # ragged single chunk (125 of 256 vectors)
+    wl(8, 70, 8192, eps=1e-5, std=(1 / 8) ** 0.5),
+    wl(16, 19, 2056, n_out=3),         # max partials, ragged second chunk
+    wl(8, 9, 16384, n_out=2),          # max bf16 H: 8 chunks in registers
+    wl(5, 13, 2040, n_out=8),          # max destinations
+    wl(4, 33, 5120, "f32", n_out=4, column=True),
+    wl(2, 9, 4, "f32"),                # one vector per row
+    wl(5, 21, 8192, "f32"),            # max fp32 H
+    wl(16, 7, 1028, "f32", n_out=2),   # ragged fp32 chunk
+    wl(3, 40, 6000, "f32", eps=0.5),   # large eps, 6 ragged chunks
+]
+
+
+@pytest.mark.parametrize("path", ["rows", "warp", "auto"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
+def test_parity_full_range(case, path):
+    check_workload(case, path=path)
+
+
+@pytest.mark.parametrize("path", ["rows", "warp"])
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[7]], ids=lambda c: c.name)
+def test_parity_sub_range(case, path):
+    check_workload(case, path=path, t0=3, t1=case.T - 2)
+
+
+@pytest.mark.parametrize("path", ["rows", "warp"])
+@pytest.mark.parametrize("case", [CASES[3], CASES[9]], ids=lambda c: c.name)
+def test_parity_in_place_residual(case, path):
+    check_workload(case, path=path, t0=2, t1=case.T - 1, in_place=True)
+
+
+@pytest.mark.parametrize("max_sms", [1, 2, 7])
+def test_parity_small_sm_budget(max_sms):
+    # Many tokens per CTA: the stage ring wraps around many times.
+    check_workload(wl(8, 45, 8192, n_out=2), path="rows", max_sms=max_sms)
+    check_workload(wl(3, 30, 1000), path="warp", max_sms=max_sms)
+
+
+def test_parity_traditional_order():
+    check_workload(CASES[3], order="traditional")
+
+
+@pytest.mark.parametrize("path", ["rows", "warp"])
+def test_single_token_and_empty_range(path):
+    check_workload(wl(8, 1, 8192), path=path)
+    check_workload(wl(2, 6, 64), path=path, t0=4, t1=4)   # no-op: nothing written
+    check_workload(wl(2, 6, 64), path=path, t0=5, t1=6)   # last row only
+
+
+def test_split_launch_parity():
+    case = wl(8, 64, 8192)
+    for t_split in (0, 1, 31, 64):
+        check_workload(case, split=t_split)
+
+
+def test_device_status_clean():
+    from reduce_residual_rmsnorm_tw_gb300 import tw
+    check_workload(CASES[1], path="rows")
+    torch.cuda.synchronize()
+    assert tw.tw_device_status() == 0

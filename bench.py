@@ -1,0 +1,503 @@
+"""Benchmark of the fused reduce + residual add + RMSNorm step on GB300.
+
+One step = one launch of the fused kernel over one batch of the headline
+workload (N=8 dense row-parallel bf16 partials, T=1024 tokens, H=8192), with
+inputs already resident in HBM.  Prints ONE JSON line (rank 0):
+
+  value     tokens/s over all ranks (device time, CUDA events, max over ranks)
+  roofline  achieved algorithmic GB/s of the kernel vs the measured HBM copy
+            peak; algorithmic bytes per token = (N + 1 + n_out + 1) * H * 2
+  e2e       the same metric through the C ABI with pinned HOST buffers: every
+            step copies its inputs host->device, runs the kernel and copies the
+            outputs back, all inside the timed region
+  cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
+  sm_budget the same kernel held to 8 SMs
+
+L2 (129 MB) is defeated by rotating through several buffer sets whose total
+is above 3x the L2 size, so every step streams from HBM.
+
+--impl reference times the oracle (the only reference this path has) on the
+host cores instead.  --sweep adds the SM-budget sweep, the decode sweep, the
+two-stream split and the fp32 column-split workload as extra fields.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused reduce+add+RMSNorm tokens/s and HBM GB/s (% of roofline) on 1 GB300"
+HEADLINE = "tp8_t1024_h8192_bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["tw", "reference"], default="tw")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    """Hash of the kernel sources: a stored ncu traffic figure is only
+    reported while it still describes the kernel being timed."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_tw_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload):
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]),
+                "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows
+                                                         if r[2].strip() not in ("", "[N/A]")),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------ workloads ---
+class Resident:
+    """n_sets batches of a workload resident in HBM as ONE [n_sets * T, H]
+    allocation per tensor; batch i is token range [i*T, (i+1)*T).  Rotating
+    through the batches keeps every step streaming from HBM: the sets total
+    more than 3x the L2 size."""
+
+    def __init__(self, wl, min_sets=2):
+        import torch
+        from reduce_residual_rmsnorm_tw_gb300 import inputs
+        l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or (132 << 20)
+        per_set = wl.bytes_per_token() * wl.T
+        self.n_sets = max(min_sets, -(-3 * l2 // per_set))
+        self.l2_bytes = l2
+        self.wl = wl
+        self.big = wl.with_tokens(wl.T * self.n_sets)
+        d = inputs.make_inputs(self.big, device="cuda")
+        self.partials, self.residual, self.weight = d["partials"], d["residual"], d["weight"]
+        self.out = [torch.empty_like(self.residual) for _ in range(wl.n_out)]
+        self.residual_out = torch.empty_like(self.residual)
+
+    def ranges(self):
+        T = self.wl.T
+        return [(i * T, (i + 1) * T) for i in range(self.n_sets)]
+
+    def launchers(self, max_sms=None, path="auto"):
+        from reduce_residual_rmsnorm_tw_gb300 import tw
+        return [tw.prepare(self.partials, self.residual, self.weight, self.out,
+                           self.residual_out, self.wl.eps, t0, t1, max_sms=max_sms, path=path)
+                for t0, t1 in self.ranges()]
+
+    def l2_note(self):
+        total = self.wl.bytes_per_token() * self.big.T
+        return (f"inputs larger than L2: {self.n_sets} rotating batches, "
+                f"{total / 1e6:.0f} MB total vs {self.l2_bytes / 1e6:.0f} MB L2")
+
+
+def time_launches(launchers, steps, warmup, stream, sync_ranks=None):
+    """Launch launchers[i % n] for warmup + steps steps on `stream`; the timed
+    steps are bracketed by CUDA events per launch and around the region.
+    Returns (region_ms, per_launch_ms list)."""
+    import torch
+    n = len(launchers)
+    h = stream.cuda_stream
+    torch.cuda.synchronize()  # inputs were drawn on the default stream
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            launchers[i % n](h)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    begin = torch.cuda.Event(enable_timing=True)
+    finish = torch.cuda.Event(enable_timing=True)
+    if sync_ranks:
+        sync_ranks()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("tw_timed")  # lets ncu --nvtx-include select this region
+    with torch.cuda.stream(stream):
+        begin.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            launchers[(warmup + i) % n](h)
+            ends[i].record(stream)
+        finish.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    if sync_ranks:
+        sync_ranks()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return begin.elapsed_time(finish), per
+
+
+def summarize(per):
+    ps = sorted(per)
+    return {"mean_launch_ms": sum(ps) / len(ps), "median_launch_ms": ps[len(ps) // 2],
+            "min_launch_ms": ps[0]}
+
+
+def check_status():
+    from reduce_residual_rmsnorm_tw_gb300 import tw
+    status = tw.tw_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: a kernel gave up on a bounded wait")
+
+
+def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None):
+    """Time the fused kernel on the resident batches of `res`."""
+    import torch
+    stream = torch.cuda.Stream()
+    region_ms, per = time_launches(res.launchers(max_sms, path), steps, warmup, stream,
+                                   sync_ranks)
+    check_status()
+    return dict(region_ms=region_ms, **summarize(per))
+
+
+# ------------------------------------------------------------------ e2e ---
+def e2e_leg(wl, steps, warmup, sync_ranks=None):
+    """The same step from pinned HOST buffers: per step, copy the inputs
+    host->device, run the fused kernel through the C ABI, copy the outputs
+    device->host; all on one stream, all inside the timed region."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    d = inputs.make_inputs(wl, device="cuda")
+    h_parts = [p.cpu().pin_memory() for p in d["partials"]]
+    h_res, h_w = d["residual"].cpu().pin_memory(), d["weight"].cpu().pin_memory()
+    h_out = [torch.empty(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory() for _ in range(wl.n_out)]
+    h_res_out = torch.empty(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()
+    out = [torch.empty_like(d["residual"]) for _ in range(wl.n_out)]
+    res_out = torch.empty_like(d["residual"])
+    launch = tw.prepare(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps)
+    stream = torch.cuda.Stream()
+    h = stream.cuda_stream
+    torch.cuda.synchronize()
+
+    def step():
+        for dev, host in zip(d["partials"] + [d["residual"], d["weight"]],
+                             h_parts + [h_res, h_w]):
+            dev.copy_(host, non_blocking=True)
+        launch(h)
+        for host, dev in zip(h_out + [h_res_out], out + [res_out]):
+            host.copy_(dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    begin, finish = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sync_ranks:
+        sync_ranks()
+    with torch.cuda.stream(stream):
+        begin.record(stream)
+        for _ in range(steps):
+            step()
+        finish.record(stream)
+    torch.cuda.synchronize()
+    if sync_ranks:
+        sync_ranks()
+    check_status()
+    es = wl.elem_bytes
+    h2d = (wl.n_parts + 1) * wl.T * wl.H * es + wl.H * es
+    d2h = (wl.n_out + 1) * wl.T * wl.H * es
+    return begin.elapsed_time(finish), h2d, d2h
+
+
+# ---------------------------------------------------------- CPU oracle ---
+def oracle_sample(wl, n_tokens):
+    """fp64 inputs of the first n_tokens tokens of the workload (CPU draw)."""
+    from reduce_residual_rmsnorm_tw_gb300 import inputs
+    d = inputs.make_inputs(wl.with_tokens(n_tokens), device="cpu")
+    return ([inputs.to_f64(p) for p in d["partials"]], inputs.to_f64(d["residual"]),
+            inputs.to_f64(d["weight"]))
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle (reordered order, fp64, as it stands) on this host's cores,
+    repeated on a bounded sample of the workload for about `seconds`."""
+    import oracle
+    n_tok = min(wl.T, 64)
+    parts, res, w = oracle_sample(wl, n_tok)
+    oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)  # build + warm
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
+        runs += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= seconds:
+            break
+    return {"value": runs * n_tok / elapsed, "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"first {n_tok} tokens of {wl.name}, fp64 reordered order, "
+                      f"{runs} runs in {elapsed:.1f} s"}
+
+
+def reference_main(args):
+    """--impl reference: the oracle timed on the host cores, one bounded
+    sample of the workload per step, rank 0 only."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import oracle
+    from reduce_residual_rmsnorm_tw_gb300.inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    calib_tok = min(wl.T, 16)
+    parts, res, w = oracle_sample(wl, calib_tok)
+    oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
+    t0 = time.perf_counter()
+    oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
+    per_tok = (time.perf_counter() - t0) / calib_tok
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_tok = int(max(1, min(wl.T, budget / max(per_tok, 1e-9))))
+    parts, res, w = oracle_sample(wl, n_tok)
+    for _ in range(args.warmup):
+        oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
+    elapsed = time.perf_counter() - t0
+    value = args.steps * n_tok / elapsed
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "n_parts": wl.n_parts, "T": wl.T, "H": wl.H,
+                       "n_out": wl.n_out, "eps": wl.eps,
+                       "step": f"{n_tok} tokens of the batch per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
+                             "cores": oracle.threads(),
+                             "sample": f"{n_tok} of {wl.T} tokens per step, fp64 "
+                                       "reordered order"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- sweep ---
+def sweep(args, sync_ranks):
+    """SM-budget sweep, decode sweep, two-stream split, fp32 column split."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    W = inputs.WORKLOADS
+    peak, _ = measured_peaks()
+    out = {}
+
+    def entry(wl, ms):
+        gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
+        return {"launch_us": round(ms * 1e3, 2), "tokens_per_s": wl.T / (ms * 1e-3),
+                "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)}
+
+    steps = max(50, min(args.steps, 2000))
+    for name in (HEADLINE, "tp2_t2048_h4096_bf16"):
+        res = Resident(W[name])
+        out[f"sm_budget:{name}"] = {
+            str(b): entry(res.wl, device_leg(res, steps, 20, max_sms=b)["mean_launch_ms"])
+            for b in (2, 4, 8, 16, 148, 10 ** 6)}
+        del res
+    dec = {}
+    for T in inputs.DECODE_TOKENS:
+        res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
+        dec[str(T)] = {path: entry(res.wl, device_leg(res, steps, 20, path=path)
+                                   ["median_launch_ms"]) for path in ("warp", "rows", "auto")}
+        del res
+    out["decode_tp8_h8192_bf16"] = dec
+    # fp32 column split, four destinations.
+    res = Resident(W["colsplit_tp4_t8192_h5120_f32_out4"])
+    out["colsplit_tp4_t8192_h5120_f32_out4"] = entry(
+        res.wl, device_leg(res, max(20, steps // 20), 5)["mean_launch_ms"])
+    del res
+    # Two-chunk split on two streams (fork/join inside the library).
+    wl = W["split_tp8_t16384_h8192_bf16"]
+    res = Resident(wl)
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    split = {}
+    for b in (2, 4, 8, 16, 148):
+        n_rep = 3 if b <= 4 else 20
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for rep in range(n_rep + 1):
+            if rep == 1:
+                evs[0].record(s0)
+            t0, t1 = res.ranges()[rep % res.n_sets]
+            parts = [p[t0:t1] for p in res.partials]
+            tw.tw_split_launch(parts, res.residual[t0:t1], res.weight,
+                               [o[t0:t1] for o in res.out], res.residual_out[t0:t1],
+                               wl.eps, t_split=-1, max_sms=b, s0=s0, s1=s1)
+        evs[1].record(s0)
+        torch.cuda.synchronize()
+        split[str(b)] = entry(wl, evs[0].elapsed_time(evs[1]) / n_rep)
+    check_status()
+    out["split_tp8_t16384_h8192_bf16"] = split
+    return out
+
+
+# ------------------------------------------------------------------ main ---
+def max_over_ranks(values, world):
+    """Element-wise max of a list of floats over all ranks (host-side gloo
+    all-reduce; the data path itself has no collective)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tokens_per_s(world, tokens_per_step, steps, max_region_ms):
+    """Replicas: every rank processes its own batch each step (weak scaling)."""
+    return world * tokens_per_step * steps / (max_region_ms * 1e-3)
+
+
+def tw_main(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    sync_ranks = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")  # host-side barrier and timing reduce only
+        sync_ranks = dist.barrier
+    if rank == 0:
+        from reduce_residual_rmsnorm_tw_gb300 import build as twbuild
+        twbuild.build()
+    if sync_ranks:
+        sync_ranks()
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    tw.load()
+    wl = inputs.WORKLOADS[args.workload]
+    res = Resident(wl)
+    l2_note = res.l2_note()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    dev = device_leg(res, args.steps, args.warmup, sync_ranks=sync_ranks)
+    clocks = sampler.stop() if sampler else None
+
+    region_ms, launch_ms = max_over_ranks([dev["region_ms"], dev["mean_launch_ms"]], world)
+    value = whole_job_tokens_per_s(world, wl.T, args.steps, region_ms)
+    peak, peak_kind = measured_peaks()
+    algo_bytes = wl.bytes_per_token() * wl.T
+    achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
+
+    sm8 = device_leg(res, max(50, min(args.steps, 2000)), 20, max_sms=8)
+    sm8_gbs = algo_bytes / (sm8["mean_launch_ms"] * 1e-3) / 1e9
+    del res
+    torch.cuda.empty_cache()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(10, min(200, args.steps // 100))
+        e2e_ms, h2d, d2h = e2e_leg(wl, e2e_steps, 3, sync_ranks)
+        (e2e_ms,) = max_over_ranks([e2e_ms], world)
+        e2e = {"value": whole_job_tokens_per_s(world, wl.T, e2e_steps, e2e_ms),
+               "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "path": "pinned host -> HBM copies, kernel, HBM -> host "
+                                            "copies on one stream"}
+    extra = sweep(args, None) if args.sweep and rank == 0 else None
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "n_parts": wl.n_parts, "T": wl.T, "H": wl.H,
+                   "n_out": wl.n_out, "eps": wl.eps, "l2": l2_note,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "sm_count": torch.cuda.get_device_properties(local_rank).multi_processor_count},
+        "hbm_gbs": round(achieved, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": stored_traffic(wl.name), "peak_kind": peak_kind,
+                     "frac_of_8tbs": round(achieved / 8000.0, 4),
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "mean_launch_us": round(launch_ms * 1e3, 2),
+                     "median_launch_us": round(dev["median_launch_ms"] * 1e3, 2)},
+        "sm_budget_8": {"tokens_per_s": wl.T / (sm8["mean_launch_ms"] * 1e-3),
+                        "gbs": round(sm8_gbs, 1), "frac": round(sm8_gbs / peak, 4)},
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks,
+    }
+    if extra is not None:
+        line["sweep"] = extra
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return reference_main(args)
+    return tw_main(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

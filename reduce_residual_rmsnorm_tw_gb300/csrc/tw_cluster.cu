@@ -1,0 +1,219 @@
+// tw_cluster.cu -- the cluster kernel: one token per thread-block cluster, for
+// decode-size ranges where a single warp or CTA per token leaves most of the
+// GPU idle and a token's 100+ KB must arrive in one memory round trip.
+//
+// Same arithmetic as the other kernels ("TokenWeave 策略详解", §1 背景 and §5
+// 融合内核): x = (sum_r partials[r]) + residual in fp32, ranks in order;
+// residual_out = x; out[k] = x / sqrt(mean x^2 + eps) * weight.
+//
+// The C CTAs of a cluster split the token's columns into C contiguous slices.
+// Each thread issues all N + 1 loads of its vectors at once, sums them, and
+// the CTA's partial sum of squares is exchanged through distributed shared
+// memory: every CTA publishes its total in its own shared memory, one cluster
+// barrier makes them visible, and every thread adds the C totals in rank order
+// (so all CTAs get the same bits).  No global scratch and no multicast.
+#include "tw_device.cuh"
+
+namespace tw {
+namespace {
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Full cluster barrier: release this CTA's shared-memory writes, acquire the
+// peers'.  All CTAs of a cluster are co-scheduled, so it always completes.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// same offset as `local` in this CTA.
+__device__ __forceinline__ float ld_peer_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(smem_addr(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kClusterThreads)
+    cluster_kernel(const __grid_constant__ Params p) {
+    using V = Vec<T>;
+    constexpr int E = V::kElems;
+    constexpr int kWarps = kClusterThreads / 32;
+    __shared__ float warp_part[kWarps];
+    __shared__ float cta_part[2];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t crank = cluster_rank();
+    const uint32_t csize = cluster_size();
+    if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
+
+    const int64_t nvec = p.row_bytes / 16;
+    const int64_t per_cta = (nvec + csize - 1) / csize;
+    const int64_t v_begin = static_cast<int64_t>(crank) * per_cta;
+    const int64_t v_end = v_begin + per_cta < nvec ? v_begin + per_cta : nvec;
+
+    uint4 wv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int64_t v = v_begin + tid + k * kClusterThreads;
+        wv[k] = v < v_end ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
+                          : make_uint4(0, 0, 0, 0);
+    }
+
+    int buf = 0;
+    for (int64_t t = p.t0 + cluster_index(); t < p.t1; t += cluster_count()) {
+        const int64_t row_off = t * p.row_bytes;
+        float x[VPT][E];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = v_begin + tid + k * kClusterThreads;
+            const bool valid = v < v_end;
+            uint4 raw[TW_MAX_PARTS];
+#pragma unroll
+            for (int r = 0; r < TW_MAX_PARTS; ++r)
+                raw[r] = (valid && r < p.n_parts)
+                             ? ld_global_nc(static_cast<const char*>(p.partials[r]) + row_off +
+                                            v * 16)
+                             : make_uint4(0, 0, 0, 0);
+            const uint4 res = valid ? ld_global(static_cast<const char*>(p.residual) + row_off +
+                                                v * 16)
+                                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[k][e] = 0.f;
+#pragma unroll
+            for (int r = 0; r < TW_MAX_PARTS; ++r) {
+                if (r < p.n_parts) {
+                    float f[E];
+                    V::to_float(raw[r], f);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[k][e] += f[e];
+                }
+            }
+            float f[E];
+            V::to_float(res, f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                x[k][e] += f[e];
+                ss = fmaf(x[k][e], x[k][e], ss);
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) warp_part[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s += warp_part[w];
+            cta_part[buf] = s;
+        }
+        cluster_sync();
+        float total = 0.f;
+        for (uint32_t r = 0; r < csize; ++r) total += ld_peer_f32(&cta_part[buf], r);
+        buf ^= 1;
+        const float inv = rsqrtf(total * p.inv_H + p.eps);
+
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = v_begin + tid + k * kClusterThreads;
+            if (v < v_end) {
+                const int64_t off = row_off + v * 16;
+                st_global_cs(static_cast<char*>(p.residual_out) + off, V::from_float(x[k]));
+                float w[E], y[E];
+                V::to_float(wv[k], w);
+#pragma unroll
+                for (int e = 0; e < E; ++e) y[e] = (x[k][e] * inv) * w[e];
+                const uint4 packed = V::from_float(y);
+                for (int o = 0; o < p.n_out; ++o)
+                    st_global_cs(static_cast<char*>(p.out[o]) + off, packed);
+            }
+        }
+    }
+    // No CTA may leave while a peer can still read its shared memory.
+    cluster_sync();
+}
+
+template <typename T>
+void* cluster_entry_for(int vpt) {
+    switch (vpt) {
+        case 1: return reinterpret_cast<void*>(&cluster_kernel<T, 1>);
+        case 2: return reinterpret_cast<void*>(&cluster_kernel<T, 2>);
+        case 4: return reinterpret_cast<void*>(&cluster_kernel<T, 4>);
+        default: return nullptr;
+    }
+}
+
+void* cluster_kernel_for(int dtype, int vpt) {
+    return dtype == TW_BF16 ? cluster_entry_for<__nv_bfloat16>(vpt) : cluster_entry_for<float>(vpt);
+}
+
+}  // namespace
+
+int cluster_vectors_per_thread(int64_t row_bytes, int cluster) {
+    const int64_t nvec = row_bytes / 16;
+    const int64_t per_cta = (nvec + cluster - 1) / cluster;
+    const int64_t need = (per_cta + kClusterThreads - 1) / kClusterThreads;
+    for (int v = 1; v <= kClusterMaxVpt; v *= 2)
+        if (v >= need) return v;
+    return 0;
+}
+
+int cluster_set_attributes(int smem_optin) {
+    for (int dt = 0; dt < 2; ++dt)
+        for (int v = 1; v <= kClusterMaxVpt; v *= 2) {
+            void* fn = cluster_kernel_for(dt, v);
+            cudaError_t e = cudaFuncSetAttribute(
+                fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return static_cast<int>(e);
+        }
+    return 0;
+}
+
+int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
+                   void* stream) {
+    const int vpt = cluster_vectors_per_thread(p.row_bytes, cluster);
+    void* fn = cluster_kernel_for(dtype, vpt);
+    if (!fn) return static_cast<int>(cudaErrorInvalidValue);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster * n_clusters));
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {const_cast<Params*>(&p)};
+    return static_cast<int>(cudaLaunchKernelExC(&cfg, fn, args));
+}
+
+}  // namespace tw

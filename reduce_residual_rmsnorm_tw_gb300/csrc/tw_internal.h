@@ -22,6 +22,10 @@ constexpr int kMinStages = 2;
 constexpr int kExclusiveSmemBytes = 120 * 1024;
 // Warps per CTA of the warp-per-token kernel.
 constexpr int kWarpTokensPerCta = 4;
+// Cluster kernel: threads per CTA, largest cluster, vectors per thread bound.
+constexpr int kClusterThreads = 128;
+constexpr int kClusterMaxSize = 16;
+constexpr int kClusterMaxVpt = 4;
 
 struct Params {
     const void* partials[TW_MAX_PARTS];
@@ -50,5 +54,10 @@ size_t rows_smem_bytes(int n_parts, int stages);
 // current device (cudaError_t as int).
 int rows_set_smem_limit(int smem_optin);
 int warp_set_smem_limit(int smem_optin);
+int cluster_set_attributes(int smem_optin);
+// Vectors per thread the cluster kernel needs (0: the row is too long).
+int cluster_vectors_per_thread(int64_t row_bytes, int cluster);
+int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
+                   void* stream);
 
 }  // namespace tw

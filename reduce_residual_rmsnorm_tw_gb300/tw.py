@@ -191,3 +191,35 @@ def tw_last_error_string():
 
 def tw_version():
     return load().tw_version()
+
+
+class Prepared:
+    """A tw_fused_reduce_add_rmsnorm_ex call with its arguments marshalled
+    once, for launch loops where per-call Python work would outlast the
+    kernel.  The tensors must stay alive and unchanged in shape."""
+
+    def __init__(self, partials, residual, weight, out, residual_out, eps, t0=0,
+                 t1=None, max_sms=None, path="auto"):
+        p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                    out, residual_out)
+        self._keep = (p_arr, o_arr, list(partials), residual, weight, list(out),
+                      residual_out)
+        self._fn = load().tw_fused_reduce_add_rmsnorm_ex
+        self._args = [p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr,
+                      n_out, residual_out.data_ptr(), T, H, eps, t0,
+                      T if t1 is None else t1,
+                      _ALL_SMS if max_sms is None else max_sms]
+        self._tail = [dt, PATHS[path], None]
+
+    def __call__(self, stream_handle):
+        """Launch on the raw cudaStream_t handle (an int)."""
+        rc = self._fn(*self._args, stream_handle, *self._tail)
+        if rc != 0:
+            _check(rc)
+
+
+def prepare(partials, residual, weight, out, residual_out, eps, t0=0, t1=None,
+            max_sms=None, path="auto"):
+    """Marshal a fused call once; returns a :class:`Prepared` callable."""
+    return Prepared(partials, residual, weight, out, residual_out, eps, t0, t1,
+                    max_sms, path)

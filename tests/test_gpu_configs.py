@@ -38,6 +38,9 @@ def test_split_t16384_sampled(max_sms):
     d = inputs.make_inputs(wl, device="cuda")
     out, res_out = alloc_outputs(wl)
     s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    # Side streams are non-blocking: order s0 after the input draw and the
+    # sentinel fill on the current stream (the library orders s1 after s0).
+    s0.wait_stream(torch.cuda.current_stream())
     tw.tw_split_launch(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps,
                        t_split=-1, max_sms=max_sms, s0=s0, s1=s1)
     s0.synchronize()

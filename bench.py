@@ -361,13 +361,24 @@ def sweep(args, sync_ranks):
     for T in inputs.DECODE_TOKENS:
         res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
         dec[str(T)] = {path: entry(res.wl, device_leg(res, steps, 20, path=path)
-                                   ["median_launch_ms"]) for path in ("warp", "rows", "auto")}
+                                   ["median_launch_ms"])
+                       for path in ("warp", "cluster", "rows", "auto")}
         del res
     out["decode_tp8_h8192_bf16"] = dec
-    # fp32 column split, four destinations.
+    # fp32 column split, four destinations: the dense read of all N zero-padded
+    # partials, and the column-split mode that reads each rank's slice only
+    # (GB/s counted against the dense algorithmic bytes; the column-split
+    # algorithmic bytes per token are (1 + 1 + n_out + 1) * H * 4).
     res = Resident(W["colsplit_tp4_t8192_h5120_f32_out4"])
-    out["colsplit_tp4_t8192_h5120_f32_out4"] = entry(
-        res.wl, device_leg(res, max(20, steps // 20), 5)["mean_launch_ms"])
+    cs = {}
+    for mode in ("auto", "colsplit"):
+        ms = device_leg(res, max(20, steps // 20), 5, path=mode)["mean_launch_ms"]
+        cs["dense" if mode == "auto" else "colsplit"] = entry(res.wl, ms)
+    wl = res.wl
+    cs_bytes = (1 + 1 + wl.n_out + 1) * wl.H * wl.elem_bytes * wl.T
+    cs["colsplit"]["colsplit_gbs"] = round(cs_bytes / (cs["colsplit"]["launch_us"] * 1e-6) / 1e9, 1)
+    cs["colsplit"]["colsplit_frac_of_measured_hbm"] = round(cs["colsplit"]["colsplit_gbs"] / peak, 4)
+    out["colsplit_tp4_t8192_h5120_f32_out4"] = cs
     del res
     # Two-chunk split on two streams (fork/join inside the library).
     wl = W["split_tp8_t16384_h8192_bf16"]

@@ -43,6 +43,9 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  A status other than TW_OK means nothing was launched.
  *     Faults after launch surface through the stream like any CUDA error.
+ *     A launch whose max_sms covers every SM is a programmatic dependent
+ *     launch: it may start while the previous kernel on the stream drains,
+ *     but touches no global memory before that kernel has completed.
  *   - Argument rules, checked on the host before any CUDA call:
  *       partials/out arrays and every pointer in them non-NULL;
  *       1 <= n_parts <= TW_MAX_PARTS, 1 <= n_out <= TW_MAX_OUTS;
@@ -93,7 +96,12 @@ typedef enum {
     TW_PATH_AUTO = 0,  /* rows kernel, or warp kernel for decode-size ranges */
     TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
                           staged into shared memory by bulk async copies */
-    TW_PATH_WARP = 2   /* one warp per token, no shared memory */
+    TW_PATH_WARP = 2,  /* one warp per token, no shared memory */
+    TW_PATH_CLUSTER = 3 /* one thread-block cluster of C CTAs per token (C the
+                           largest power of two <= min(8, max_sms)), the sum
+                           of squares exchanged through distributed shared
+                           memory; needs H * sizeof(dtype) <= C * 8 KB, else
+                           TW_ERR_UNSUPPORTED */
 } tw_path;
 
 /* The fused step on rows [t0, t1), bf16 tensors.  At most max_sms CTAs are
@@ -132,6 +140,23 @@ int tw_fused_reduce_add_rmsnorm_ex(const void* const* partials, int n_parts,
                                    float eps, int64_t t0, int64_t t1,
                                    int max_sms, void* stream, int dtype,
                                    int path, uint32_t* smid_log);
+
+/* Column-split partials ("TokenWeave 策略详解", appendix 实现方法：零填充 +
+ * AllReduce 求和 and 数值示例): partial r is the zero-padded output of rank r,
+ * nonzero only in columns [floor(r*H/n_parts), floor((r+1)*H/n_parts)), so the
+ * sum over ranks is the concatenation of those slices.  Same computation and
+ * arguments as tw_fused_reduce_add_rmsnorm, but only each rank's own slice is
+ * read (the zero columns are never touched); the result is bit-identical to
+ * the dense call on such inputs (adding zeros is exact).  Traffic per token:
+ * (1 + 1 + n_out + 1) rows instead of (n_parts + 1 + n_out + 1).  Additional
+ * rule: every slice boundary floor(r*H/n_parts) * sizeof(dtype) is a multiple
+ * of 16 bytes (else TW_ERR_ALIGNMENT).  Runs on the rows kernel. */
+int tw_fused_reduce_add_rmsnorm_colsplit(const void* const* partials, int n_parts,
+                                         const void* residual, const void* weight,
+                                         void* const* out, int n_out,
+                                         void* residual_out, int64_t T, int64_t H,
+                                         float eps, int64_t t0, int64_t t1,
+                                         int max_sms, void* stream, int dtype);
 
 /* Two-chunk token split ("Der intelligente Split"): rows [0, t_split) run on
  * stream s0 and rows [t_split, T) on stream s1, each a rows-kernel launch with

@@ -34,8 +34,10 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(TW_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-// Under TW_PATH_AUTO, token ranges of at most this many tokens (decode-size
-// batches) go to the warp kernel, larger ones to the rows kernel.
+// Under TW_PATH_AUTO, token ranges of at most kClusterPathMaxTokens tokens go
+// to the cluster kernel (one cluster per token), ranges of at most
+// kWarpPathMaxTokens to the warp kernel, larger ones to the rows kernel.
+constexpr int64_t kClusterPathMaxTokens = 16;
 constexpr int64_t kWarpPathMaxTokens = 32;
 
 struct DeviceState {
@@ -76,7 +78,8 @@ int device_state(DeviceState** out) {
             return fail(TW_ERR_UNSUPPORTED, "device %d allows only %d bytes of shared memory",
                         dev, d.smem_optin);
         if ((e = static_cast<cudaError_t>(rows_set_smem_limit(d.smem_optin))) != cudaSuccess ||
-            (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess)
+            (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess ||
+            (e = static_cast<cudaError_t>(cluster_set_attributes(d.smem_optin))) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute");
         if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)) !=
             cudaSuccess)
@@ -103,6 +106,7 @@ struct Args {
     int64_t t0, t1;
     int max_sms;
     int dtype;
+    int colsplit = 0;
 };
 
 size_t elem_size(int dtype) { return dtype == TW_BF16 ? 2 : 4; }
@@ -154,6 +158,14 @@ int check_args(const Args& a) {
     for (int k = 0; k < a.n_out; ++k)
         if (misaligned(a.out[k])) return fail(TW_ERR_ALIGNMENT, "out[%d] is not 16-byte aligned", k);
 
+    if (a.colsplit) {
+        // Each rank's column slice must start and end on a 16-byte boundary.
+        for (int r = 0; r <= a.n_parts; ++r)
+            if (((a.H * r / a.n_parts) * static_cast<int64_t>(es)) % 16 != 0)
+                return fail(TW_ERR_ALIGNMENT, "column slice %d of H %lld over %d ranks does not "
+                            "start on a 16-byte boundary", r, (long long)a.H, a.n_parts);
+    }
+
     // Aliasing: outputs against inputs and against each other.
     const size_t tb = static_cast<size_t>(a.T) * static_cast<size_t>(a.H) * es;
     const size_t wb = static_cast<size_t>(a.H) * es;
@@ -193,6 +205,9 @@ Params make_params(const Args& a, const DeviceState& d, int64_t t0, int64_t t1,
     p.n_parts = a.n_parts;
     p.n_out = a.n_out;
     p.n_chunks = static_cast<int>((p.row_bytes + kChunkBytes - 1) / kChunkBytes);
+    p.colsplit = a.colsplit;
+    const int64_t es = static_cast<int64_t>(elem_size(a.dtype));
+    for (int r = 0; r <= a.n_parts; ++r) p.col_lo[r] = (a.H * r / a.n_parts) * es;
     p.eps = a.eps;
     p.inv_H = static_cast<float>(1.0 / static_cast<double>(a.H));
     return p;
@@ -203,25 +218,50 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
                  uint32_t* smid_log, void* stream) {
     const int64_t tokens = t1 - t0;
     const int64_t sms = a.max_sms < d.sm_count ? a.max_sms : d.sm_count;
+    // A launch that may use every SM overlaps its start with the previous
+    // kernel's drain; a budgeted launch does not, so that at no time more than
+    // max_sms SMs hold its CTAs.
+    const bool pdl = a.max_sms >= d.sm_count;
     Params p = make_params(a, d, t0, t1, smid_log);
-    if (path == TW_PATH_AUTO) path = tokens <= kWarpPathMaxTokens ? TW_PATH_WARP : TW_PATH_ROWS;
+    // Largest power-of-two cluster within the budget (at most 8: portable).
+    int cluster = 1;
+    while (cluster * 2 <= 8 && cluster * 2 <= sms) cluster *= 2;
+    const bool cluster_ok = cluster_vectors_per_thread(p.row_bytes, cluster) != 0;
+    if (a.colsplit) {
+        if (path != TW_PATH_AUTO && path != TW_PATH_ROWS)
+            return fail(TW_ERR_UNSUPPORTED, "the column-split mode runs on the rows kernel only");
+        path = TW_PATH_ROWS;
+    }
+    if (path == TW_PATH_AUTO)
+        path = (tokens <= kClusterPathMaxTokens && cluster_ok) ? TW_PATH_CLUSTER
+               : tokens <= kWarpPathMaxTokens                  ? TW_PATH_WARP
+                                                               : TW_PATH_ROWS;
 
     int err;
     if (path == TW_PATH_ROWS) {
-        const size_t stage = static_cast<size_t>(a.n_parts + 1) * kChunkBytes;
-        int stages = static_cast<int>((static_cast<size_t>(d.smem_optin) - rows_smem_bytes(a.n_parts, 0)) / stage);
+        const int staged = rows_staged_rows(a.n_parts, a.colsplit);
+        const size_t stage = static_cast<size_t>(staged) * kChunkBytes;
+        int stages = static_cast<int>(
+            (static_cast<size_t>(d.smem_optin) - rows_smem_bytes(staged, 0)) / stage);
         if (stages > kMaxStages) stages = kMaxStages;
         if (stages < kMinStages)
             return fail(TW_ERR_UNSUPPORTED, "shared memory too small for %d partials", a.n_parts);
         p.stages = stages;
-        size_t smem = rows_smem_bytes(a.n_parts, stages);
+        size_t smem = rows_smem_bytes(staged, stages);
         if (smem < static_cast<size_t>(kExclusiveSmemBytes)) smem = kExclusiveSmemBytes;
         const int grid = static_cast<int>(tokens < sms ? tokens : sms);
-        err = launch_rows(p, a.dtype, grid, smem, stream);
+        err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
     } else if (path == TW_PATH_WARP) {
         const int64_t ctas = (tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta;
         const int grid = static_cast<int>(ctas < sms ? ctas : sms);
-        err = launch_warp(p, a.dtype, grid, kExclusiveSmemBytes, stream);
+        err = launch_warp(p, a.dtype, grid, kExclusiveSmemBytes, pdl, stream);
+    } else if (path == TW_PATH_CLUSTER) {
+        if (!cluster_ok)
+            return fail(TW_ERR_UNSUPPORTED, "row of %lld bytes too long for a cluster of %d",
+                        (long long)p.row_bytes, cluster);
+        const int64_t max_clusters = sms / cluster;
+        const int n_clusters = static_cast<int>(tokens < max_clusters ? tokens : max_clusters);
+        err = launch_cluster(p, a.dtype, cluster, n_clusters, kExclusiveSmemBytes, pdl, stream);
     } else {
         return fail(TW_ERR_INVALID_ARG, "unknown path %d", path);
     }
@@ -232,7 +272,7 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 int fused(const Args& a, int path, uint32_t* smid_log, void* stream) {
     int rc = check_args(a);
     if (rc != TW_OK) return rc;
-    if (path < TW_PATH_AUTO || path > TW_PATH_WARP)
+    if (path < TW_PATH_AUTO || path > TW_PATH_CLUSTER)
         return fail(TW_ERR_INVALID_ARG, "unknown path %d", path);
     if (a.t0 == a.t1) return TW_OK;
     DeviceState* d = nullptr;
@@ -255,6 +295,17 @@ int tw_fused_reduce_add_rmsnorm_ex(const void* const* partials, int n_parts,
     const Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
                  T,        H,       eps,      t0,     t1,  max_sms, dtype};
     return tw::fused(a, path, smid_log, stream);
+}
+
+int tw_fused_reduce_add_rmsnorm_colsplit(const void* const* partials, int n_parts,
+                                         const void* residual, const void* weight,
+                                         void* const* out, int n_out, void* residual_out,
+                                         int64_t T, int64_t H, float eps, int64_t t0, int64_t t1,
+                                         int max_sms, void* stream, int dtype) {
+    Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+           T,        H,       eps,      t0,     t1,  max_sms, dtype};
+    a.colsplit = 1;
+    return tw::fused(a, TW_PATH_ROWS, nullptr, stream);
 }
 
 int tw_fused_reduce_add_rmsnorm(const void* const* partials, int n_parts, const void* residual,

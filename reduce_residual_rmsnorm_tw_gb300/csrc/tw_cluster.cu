@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kClusterThreads)
     const int lane = tid & 31;
     const uint32_t crank = cluster_rank();
     const uint32_t csize = cluster_size();
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
 
     const int64_t nvec = p.row_bytes / 16;
@@ -196,7 +198,7 @@ int cluster_set_attributes(int smem_optin) {
 }
 
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
-                   void* stream) {
+                   bool pdl, void* stream) {
     const int vpt = cluster_vectors_per_thread(p.row_bytes, cluster);
     void* fn = cluster_kernel_for(dtype, vpt);
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
@@ -205,13 +207,15 @@ int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size
     cfg.blockDim = dim3(kClusterThreads);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     void* args[] = {const_cast<Params*>(&p)};
     return static_cast<int>(cudaLaunchKernelExC(&cfg, fn, args));
 }

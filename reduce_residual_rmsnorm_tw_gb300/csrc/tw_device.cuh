@@ -104,6 +104,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Programmatic dependent launch.  wait: block until the grids this launch
+// depends on have completed and their memory is visible (a no-op when the
+// launch had no programmatic dependency).  launch_dependents: allow the next
+// grid of the stream to begin launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over `threads` threads (a multiple of 32), id != 0.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -151,6 +162,50 @@ struct Vec<float> {
     }
 };
 
+// acc[e] += element e of the 16-byte vector v, in fp32 with one rounding per
+// add (the same bits as widening the element and adding).  bf16 elements go
+// through the mixed-precision add (the bf16 operand is widened exactly);
+// fp32 pairs through the packed two-lane add.
+__device__ __forceinline__ void add_vec(float (&acc)[8], const uint4& v, __nv_bfloat16*) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\t"
+            "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "r"(w[i]));
+}
+__device__ __forceinline__ void add_vec(float (&acc)[4], const uint4& v, float*) {
+    asm("{\n\t.reg .b64 a, b;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 a, a, b;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%6, %7};\n\t"
+        "add.rn.f32x2 a, a, b;\n\t"
+        "mov.b64 {%2, %3}, a;\n\t}"
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+// ss2 += x * x on two lanes at a time (packed fp32 FMA); the caller adds the
+// two lanes at the end.
+template <int E>
+__device__ __forceinline__ void sum_squares(float (&ss2)[2], const float (&x)[E]) {
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+        asm("{\n\t.reg .b64 a, s;\n\t"
+            "mov.b64 a, {%2, %3};\n\t"
+            "mov.b64 s, {%0, %1};\n\t"
+            "fma.rn.f32x2 s, a, a, s;\n\t"
+            "mov.b64 {%0, %1}, s;\n\t}"
+            : "+f"(ss2[0]), "+f"(ss2[1])
+            : "f"(x[e]), "f"(x[e + 1]));
+}
+
 // Streaming 16-byte global store (written once, not re-read by this kernel).
 __device__ __forceinline__ void st_global_cs(void* p, const uint4& v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
@@ -176,6 +231,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Host side: launch fn(p) with the given shape, optionally with programmatic
+// stream serialization (see grid_dependency_wait).  Returns a cudaError_t.
+inline int launch_with_pdl(void* fn, const Params& p, int grid, int block, size_t smem_bytes,
+                           bool pdl, void* stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void* args[] = {const_cast<Params*>(&p)};
+    return static_cast<int>(cudaLaunchKernelExC(&cfg, fn, args));
 }
 
 }  // namespace tw

@@ -11,6 +11,8 @@ namespace tw {
 // staged chunk, so a chunk row is kRowsThreads * 16 bytes.
 constexpr int kRowsThreads = 256;
 constexpr int kChunkBytes = kRowsThreads * 16;
+// Consumer groups of the rows kernel: group g sums the chunks c = g mod kRowsGroups.
+constexpr int kRowsGroups = 2;
 // Chunks per token the rows kernel keeps in registers (H <= 8 * 4 KB bytes).
 constexpr int kMaxChunks = 8;
 // Ring depth bounds of the rows kernel.
@@ -38,18 +40,29 @@ struct Params {
     int64_t t0, t1;         // token range
     int64_t row_bytes;      // H * element size (multiple of 16)
     int64_t H;
+    // Column-split mode (rows kernel): partial r is zero outside the byte
+    // range [col_lo[r], col_lo[r + 1]) of each row, which alone is read; the
+    // staged chunk then holds the concatenation in one row.
+    int64_t col_lo[TW_MAX_PARTS + 1];
     int n_parts, n_out;
     int n_chunks;           // ceil(row_bytes / kChunkBytes), rows kernel
     int stages;             // ring depth, rows kernel
+    int colsplit;           // 1: column-split mode
     float eps;
     float inv_H;
 };
 
-// Launchers (return a cudaError_t value as int).
-int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, void* stream);
-int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, void* stream);
-// Shared memory the rows kernel needs for a given ring depth.
-size_t rows_smem_bytes(int n_parts, int stages);
+// Launchers (return a cudaError_t value as int).  `pdl` launches with
+// programmatic stream serialization: the kernel may start while the previous
+// kernel of the stream drains, and waits (griddepcontrol.wait) before its
+// first global memory access.
+int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
+                void* stream);
+int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
+                void* stream);
+// Rows staged per ring stage and shared memory of a ring depth.
+int rows_staged_rows(int n_parts, int colsplit);
+size_t rows_smem_bytes(int staged_rows, int stages);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).
 int rows_set_smem_limit(int smem_optin);
@@ -58,6 +71,6 @@ int cluster_set_attributes(int smem_optin);
 // Vectors per thread the cluster kernel needs (0: the row is too long).
 int cluster_vectors_per_thread(int64_t row_bytes, int cluster);
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
-                   void* stream);
+                   bool pdl, void* stream);
 
 }  // namespace tw

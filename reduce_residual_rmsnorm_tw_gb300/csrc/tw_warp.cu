@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kWarpTokensPerCta * 32)
     using V = Vec<T>;
     constexpr int E = V::kElems;
     const int lane = threadIdx.x & 31;
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (threadIdx.x == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
 
     const int64_t nvec = p.row_bytes / 16;
@@ -135,11 +137,10 @@ int warp_set_smem_limit(int smem_optin) {
     return 0;
 }
 
-int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, void* stream) {
-    void* args[] = {const_cast<Params*>(&p)};
-    return static_cast<int>(cudaLaunchKernel(warp_kernel_for(dtype), dim3(grid),
-                                             dim3(kWarpTokensPerCta * 32), args, smem_bytes,
-                                             static_cast<cudaStream_t>(stream)));
+int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
+                void* stream) {
+    return launch_with_pdl(warp_kernel_for(dtype), p, grid, kWarpTokensPerCta * 32, smem_bytes,
+                           pdl, stream);
 }
 
 }  // namespace tw

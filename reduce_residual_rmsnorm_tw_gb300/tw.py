@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtw.so")
 
 TW_BF16, TW_F32 = 0, 1
-PATHS = {"auto": 0, "rows": 1, "warp": 2}
+PATHS = {"auto": 0, "rows": 1, "warp": 2, "cluster": 3}
 MAX_PARTS, MAX_OUTS = 16, 8
 STATUS_NAMES = {0: "TW_OK", -1: "TW_ERR_INVALID_ARG", -2: "TW_ERR_ALIGNMENT",
                 -3: "TW_ERR_ALIAS", -4: "TW_ERR_CUDA", -5: "TW_ERR_UNSUPPORTED"}
@@ -51,6 +51,7 @@ def load():
     for name, extra in (("tw_fused_reduce_add_rmsnorm_bf16", []),
                         ("tw_fused_reduce_add_rmsnorm_f32", []),
                         ("tw_fused_reduce_add_rmsnorm", [ctypes.c_int]),
+                        ("tw_fused_reduce_add_rmsnorm_colsplit", [ctypes.c_int]),
                         ("tw_fused_reduce_add_rmsnorm_ex",
                          [ctypes.c_int, ctypes.c_int, vp])):
         fn = getattr(lib, name)
@@ -138,6 +139,20 @@ def tw_fused_reduce_add_rmsnorm(partials, residual, weight, out, residual_out,
     _check(rc)
 
 
+def tw_fused_reduce_add_rmsnorm_colsplit(partials, residual, weight, out,
+                                         residual_out, eps, t0=0, t1=None,
+                                         max_sms=None, stream=None):
+    """The fused step for zero-padded column-split partials: partial r is
+    nonzero only in columns [r*H//N, (r+1)*H//N), and only those are read."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    rc = load().tw_fused_reduce_add_rmsnorm_colsplit(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+        _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt)
+    _check(rc)
+
+
 def _typed(name, dtype):
     def call(partials, residual, weight, out, residual_out, eps, t0=0, t1=None,
              max_sms=None, stream=None):
@@ -204,12 +219,17 @@ class Prepared:
                                                     out, residual_out)
         self._keep = (p_arr, o_arr, list(partials), residual, weight, list(out),
                       residual_out)
-        self._fn = load().tw_fused_reduce_add_rmsnorm_ex
         self._args = [p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr,
                       n_out, residual_out.data_ptr(), T, H, eps, t0,
                       T if t1 is None else t1,
                       _ALL_SMS if max_sms is None else max_sms]
-        self._tail = [dt, PATHS[path], None]
+        if path == "colsplit":
+            # tw_fused_reduce_add_rmsnorm_colsplit: zero-padded column split.
+            self._fn = load().tw_fused_reduce_add_rmsnorm_colsplit
+            self._tail = [dt]
+        else:
+            self._fn = load().tw_fused_reduce_add_rmsnorm_ex
+            self._tail = [dt, PATHS[path], None]
 
     def __call__(self, stream_handle):
         """Launch on the raw cudaStream_t handle (an int)."""
@@ -220,6 +240,8 @@ class Prepared:
 
 def prepare(partials, residual, weight, out, residual_out, eps, t0=0, t1=None,
             max_sms=None, path="auto"):
-    """Marshal a fused call once; returns a :class:`Prepared` callable."""
+    """Marshal a fused call once; returns a :class:`Prepared` callable.
+    ``path`` is a kernel name of tw_fused_reduce_add_rmsnorm_ex, or "colsplit"
+    for tw_fused_reduce_add_rmsnorm_colsplit."""
     return Prepared(partials, residual, weight, out, residual_out, eps, t0, t1,
                     max_sms, path)

@@ -46,8 +46,12 @@ def check_untouched(t, t0, t1, what):
 
 
 def run_gpu(d, wl, out, res_out, t0, t1, path="auto", max_sms=None, split=None,
-            stream=None):
-    if split is None:
+            stream=None, colsplit=False):
+    if colsplit:
+        tw.tw_fused_reduce_add_rmsnorm_colsplit(d["partials"], d["residual"], d["weight"], out,
+                                                res_out, wl.eps, t0, t1, max_sms=max_sms,
+                                                stream=stream)
+    elif split is None:
         tw.tw_fused_reduce_add_rmsnorm_ex(d["partials"], d["residual"], d["weight"], out,
                                           res_out, wl.eps, t0, t1, max_sms=max_sms,
                                           path=path, stream=stream)
@@ -58,7 +62,7 @@ def run_gpu(d, wl, out, res_out, t0, t1, path="auto", max_sms=None, split=None,
 
 
 def check_workload(wl, path="auto", t0=0, t1=None, in_place=False, max_sms=None,
-                   split=None, order="reordered"):
+                   split=None, order="reordered", colsplit=False):
     """Full element-wise parity of one workload (inputs drawn on the CPU)."""
     t1 = wl.T if t1 is None else t1
     host = inputs.make_inputs(wl, device="cpu")
@@ -67,7 +71,8 @@ def check_workload(wl, path="auto", t0=0, t1=None, in_place=False, max_sms=None,
     out, res_out = alloc_outputs(wl)
     if in_place:
         res_out = d["residual"]  # residual_out == residual
-    run_gpu(d, wl, out, res_out, t0, t1, path=path, max_sms=max_sms, split=split)
+    run_gpu(d, wl, out, res_out, t0, t1, path=path, max_sms=max_sms, split=split,
+            colsplit=colsplit)
     torch.cuda.synchronize()
 
     fn = oracle.reordered if order == "reordered" else oracle.traditional

@@ -138,3 +138,14 @@ def test_binding_marshalling_checks():
     with pytest.raises(ValueError):
         tw.tw_fused_reduce_add_rmsnorm_f32([x], x, torch.zeros(64, dtype=torch.bfloat16),
                                            [x.clone()], x.clone(), 1e-6)
+
+
+def test_colsplit_slice_alignment(lib):
+    p_arr = (ctypes.c_void_p * 3)(BASE, BASE + MB, BASE + 2 * MB)
+    o_arr = (ctypes.c_void_p * 1)(BASE + 32 * MB)
+    # H = 4096 bf16 over 3 ranks: slice bounds 1365 and 2730 columns are not
+    # 16-byte aligned; over 2 ranks they are (checked with an empty range).
+    args = [BASE + 64 * MB, BASE + 65 * MB, o_arr, 1, BASE + 66 * MB, 4, 4096, 1e-6]
+    assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 3, *args, 0, 4, 8, None, 0) == ALIGN
+    assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 2, *args, 2, 2, 8, None, 0) == OK
+    assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 2, *args, 0, 4, 8, None, 7) == INVALID

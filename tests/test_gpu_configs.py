@@ -27,7 +27,7 @@ def test_tp8_t1024_h8192_bf16_sm_budgets(max_sms):
 
 
 @pytest.mark.parametrize("T", inputs.DECODE_TOKENS)
-@pytest.mark.parametrize("path", ["warp", "auto"])
+@pytest.mark.parametrize("path", ["warp", "cluster", "rows", "auto"])
 def test_decode_sweep_full(T, path):
     check_workload(W["decode_tp8_h8192_bf16"].with_tokens(T), path=path)
 
@@ -50,12 +50,14 @@ def test_split_t16384_sampled(max_sms):
     assert bool(torch.isfinite(res_out.float()).all())
 
 
-def test_colsplit_t8192_h5120_f32_sampled():
+@pytest.mark.parametrize("colsplit", [False, True])
+def test_colsplit_t8192_h5120_f32_sampled(colsplit):
     wl = W["colsplit_tp4_t8192_h5120_f32_out4"]
     d = inputs.make_inputs(wl, device="cuda")
     out, res_out = alloc_outputs(wl)
-    tw.tw_fused_reduce_add_rmsnorm(d["partials"], d["residual"], d["weight"], out, res_out,
-                                   wl.eps)
+    fn = (tw.tw_fused_reduce_add_rmsnorm_colsplit if colsplit
+          else tw.tw_fused_reduce_add_rmsnorm)
+    fn(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps)
     torch.cuda.synchronize()
     toks = sample_tokens(wl.T, 128, seed=4, must=(0, wl.T - 1))
     check_sampled(wl, d, out, res_out, toks)

@@ -32,19 +32,19 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("path", ["rows", "warp", "auto"])
+@pytest.mark.parametrize("path", ["rows", "warp", "cluster", "auto"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_parity_full_range(case, path):
     check_workload(case, path=path)
 
 
-@pytest.mark.parametrize("path", ["rows", "warp"])
+@pytest.mark.parametrize("path", ["rows", "warp", "cluster"])
 @pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[7]], ids=lambda c: c.name)
 def test_parity_sub_range(case, path):
     check_workload(case, path=path, t0=3, t1=case.T - 2)
 
 
-@pytest.mark.parametrize("path", ["rows", "warp"])
+@pytest.mark.parametrize("path", ["rows", "warp", "cluster"])
 @pytest.mark.parametrize("case", [CASES[3], CASES[9]], ids=lambda c: c.name)
 def test_parity_in_place_residual(case, path):
     check_workload(case, path=path, t0=2, t1=case.T - 1, in_place=True)
@@ -55,13 +55,41 @@ def test_parity_small_sm_budget(max_sms):
     # Many tokens per CTA: the stage ring wraps around many times.
     check_workload(wl(8, 45, 8192, n_out=2), path="rows", max_sms=max_sms)
     check_workload(wl(3, 30, 1000), path="warp", max_sms=max_sms)
+    # Cluster of 1, 2 or 4 CTAs: rows of up to 8 KB per CTA.
+    check_workload(wl(3, 30, 4096), path="cluster", max_sms=max_sms)
+
+
+def test_cluster_rejects_rows_too_long_for_the_budget():
+    from reduce_residual_rmsnorm_tw_gb300 import tw
+    with pytest.raises(tw.TwError, match="TW_ERR_UNSUPPORTED"):
+        check_workload(wl(2, 4, 8192), path="cluster", max_sms=1)   # 16 KB row, 1 CTA
+
+
+COLSPLIT = [
+    wl(4, 33, 5120, "f32", n_out=4, column=True),
+    wl(2, 41, 4096, n_out=2, column=True),
+    wl(8, 17, 8192, column=True),
+    wl(4, 9, 16384, column=True),
+]
+
+
+@pytest.mark.parametrize("case", COLSPLIT, ids=lambda c: c.name)
+def test_colsplit_parity_and_bits(case):
+    out, res = check_workload(case, colsplit=True)
+    dense_out, dense_res = check_workload(case, path="rows")
+    for a, b in zip(out + [res], dense_out + [dense_res]):
+        assert torch.equal(a, b), "column-split result differs from the dense rows kernel"
+
+
+def test_colsplit_sub_range_in_place():
+    check_workload(COLSPLIT[0], colsplit=True, t0=5, t1=30, in_place=True)
 
 
 def test_parity_traditional_order():
     check_workload(CASES[3], order="traditional")
 
 
-@pytest.mark.parametrize("path", ["rows", "warp"])
+@pytest.mark.parametrize("path", ["rows", "warp", "cluster"])
 def test_single_token_and_empty_range(path):
     check_workload(wl(8, 1, 8192), path=path)
     check_workload(wl(2, 6, 64), path=path, t0=4, t1=4)   # no-op: nothing written

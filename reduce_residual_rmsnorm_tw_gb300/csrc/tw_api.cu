@@ -44,6 +44,8 @@ struct DeviceState {
     bool ready = false;
     int sm_count = 0;
     int smem_optin = 0;
+    bool cluster_ready = false;
+    const char* cluster_error = "";
     unsigned int* status = nullptr;
     cudaEvent_t fork = nullptr;
     cudaEvent_t join = nullptr;
@@ -78,9 +80,16 @@ int device_state(DeviceState** out) {
             return fail(TW_ERR_UNSUPPORTED, "device %d allows only %d bytes of shared memory",
                         dev, d.smem_optin);
         if ((e = static_cast<cudaError_t>(rows_set_smem_limit(d.smem_optin))) != cudaSuccess ||
-            (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess ||
-            (e = static_cast<cudaError_t>(cluster_set_attributes(d.smem_optin))) != cudaSuccess)
+            (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute");
+        // The cluster kernel is optional: if it cannot be configured, that
+        // path reports TW_ERR_UNSUPPORTED and the others still run.
+        e = static_cast<cudaError_t>(cluster_set_attributes(d.smem_optin));
+        d.cluster_ready = e == cudaSuccess;
+        if (e != cudaSuccess) {
+            d.cluster_error = cudaGetErrorName(e);
+            (void)cudaGetLastError();  // clear the (non-sticky) launch-API error
+        }
         if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)) !=
             cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress");
@@ -226,7 +235,8 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
     // Largest power-of-two cluster within the budget (at most 8: portable).
     int cluster = 1;
     while (cluster * 2 <= 8 && cluster * 2 <= sms) cluster *= 2;
-    const bool cluster_ok = cluster_vectors_per_thread(p.row_bytes, cluster) != 0;
+    const bool cluster_ok =
+        d.cluster_ready && cluster_vectors_per_thread(p.row_bytes, cluster) != 0;
     if (a.colsplit) {
         if (path != TW_PATH_AUTO && path != TW_PATH_ROWS)
             return fail(TW_ERR_UNSUPPORTED, "the column-split mode runs on the rows kernel only");
@@ -256,6 +266,9 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
         const int grid = static_cast<int>(ctas < sms ? ctas : sms);
         err = launch_warp(p, a.dtype, grid, kExclusiveSmemBytes, pdl, stream);
     } else if (path == TW_PATH_CLUSTER) {
+        if (!d.cluster_ready)
+            return fail(TW_ERR_UNSUPPORTED, "cluster kernel unavailable on this device (%s)",
+                        d.cluster_error);
         if (!cluster_ok)
             return fail(TW_ERR_UNSUPPORTED, "row of %lld bytes too long for a cluster of %d",
                         (long long)p.row_bytes, cluster);

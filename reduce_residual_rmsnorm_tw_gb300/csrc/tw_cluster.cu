@@ -185,13 +185,14 @@ int cluster_vectors_per_thread(int64_t row_bytes, int cluster) {
 }
 
 int cluster_set_attributes(int smem_optin) {
+    // The kernel has a few bytes of static shared memory, so its dynamic
+    // request stays at the exclusive-SM amount, not the full opt-in limit.
+    if (smem_optin < kExclusiveSmemBytes + 1024) return static_cast<int>(cudaErrorInvalidValue);
     for (int dt = 0; dt < 2; ++dt)
         for (int v = 1; v <= kClusterMaxVpt; v *= 2) {
-            void* fn = cluster_kernel_for(dt, v);
-            cudaError_t e = cudaFuncSetAttribute(
-                fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            cudaError_t e = cudaFuncSetAttribute(cluster_kernel_for(dt, v),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kExclusiveSmemBytes);
             if (e != cudaSuccess) return static_cast<int>(e);
         }
     return 0;

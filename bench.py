@@ -218,52 +218,54 @@ def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None):
 
 
 # ------------------------------------------------------------------ e2e ---
-def e2e_leg(wl, steps, warmup, sync_ranks=None):
-    """The same step from pinned HOST buffers: per step, copy the inputs
-    host->device, run the fused kernel through the C ABI, copy the outputs
-    device->host; all on one stream, all inside the timed region."""
+def e2e_leg(wl, steps, warmup, chunks=(128, 256, 512), sync_ranks=None):
+    """The same step from pinned HOST buffers through the C ABI's host entry
+    point (tw_fused_reduce_add_rmsnorm_host): every step moves that step's
+    inputs host->device, runs the kernel and moves the outputs back, with the
+    copies of one token chunk overlapping the kernel on the previous chunk.
+    Returns the best chunk's (ms per step, chunk) and all chunks' ms."""
     import torch
     from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
     d = inputs.make_inputs(wl, device="cuda")
     h_parts = [p.cpu().pin_memory() for p in d["partials"]]
     h_res, h_w = d["residual"].cpu().pin_memory(), d["weight"].cpu().pin_memory()
+    del d
     h_out = [torch.empty(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory() for _ in range(wl.n_out)]
     h_res_out = torch.empty(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()
-    out = [torch.empty_like(d["residual"]) for _ in range(wl.n_out)]
-    res_out = torch.empty_like(d["residual"])
-    launch = tw.prepare(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps)
     stream = torch.cuda.Stream()
-    h = stream.cuda_stream
     torch.cuda.synchronize()
+    per_chunk = {}
+    for chunk in chunks:
+        ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk,
+                                                    wl.torch_dtype),
+                         dtype=torch.uint8, device="cuda")
 
-    def step():
-        for dev, host in zip(d["partials"] + [d["residual"], d["weight"]],
-                             h_parts + [h_res, h_w]):
-            dev.copy_(host, non_blocking=True)
-        launch(h)
-        for host, dev in zip(h_out + [h_res_out], out + [res_out]):
-            host.copy_(dev, non_blocking=True)
+        def step():
+            tw.tw_fused_reduce_add_rmsnorm_host(h_parts, h_res, h_w, h_out, h_res_out, wl.eps,
+                                                ws, chunk, stream=stream)
 
-    with torch.cuda.stream(stream):
         for _ in range(warmup):
             step()
-    torch.cuda.synchronize()
-    begin, finish = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if sync_ranks:
-        sync_ranks()
-    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        begin, finish = (torch.cuda.Event(enable_timing=True),
+                         torch.cuda.Event(enable_timing=True))
+        if sync_ranks:
+            sync_ranks()
         begin.record(stream)
         for _ in range(steps):
             step()
         finish.record(stream)
-    torch.cuda.synchronize()
-    if sync_ranks:
-        sync_ranks()
+        torch.cuda.synchronize()
+        if sync_ranks:
+            sync_ranks()
+        per_chunk[chunk] = begin.elapsed_time(finish) / steps
+        del ws
     check_status()
+    best = min(per_chunk, key=per_chunk.get)
     es = wl.elem_bytes
     h2d = (wl.n_parts + 1) * wl.T * wl.H * es + wl.H * es
     d2h = (wl.n_out + 1) * wl.T * wl.H * es
-    return begin.elapsed_time(finish), h2d, d2h
+    return per_chunk[best], best, per_chunk, h2d, d2h
 
 
 # ---------------------------------------------------------- CPU oracle ---
@@ -462,14 +464,18 @@ def tw_main(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e_steps = max(10, min(200, args.steps // 100))
-        e2e_ms, h2d, d2h = e2e_leg(wl, e2e_steps, 3, sync_ranks)
-        (e2e_ms,) = max_over_ranks([e2e_ms], world)
-        e2e = {"value": whole_job_tokens_per_s(world, wl.T, e2e_steps, e2e_ms),
-               "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": e2e_steps, "path": "pinned host -> HBM copies, kernel, HBM -> host "
-                                            "copies on one stream"}
+        e2e_steps = max(10, min(100, args.steps // 200))
+        step_ms, chunk, per_chunk, h2d, d2h = e2e_leg(wl, e2e_steps, 3, sync_ranks=sync_ranks)
+        (step_ms,) = max_over_ranks([step_ms], world)
+        e2e = {"value": whole_job_tokens_per_s(world, wl.T, 1, step_ms),
+               "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "ms_per_step": round(step_ms, 4),
+               "link_gbs": round((h2d + d2h) / (step_ms * 1e-3) / 1e9, 1),
+               "chunk_tokens": chunk,
+               "ms_per_step_by_chunk": {str(k): round(v, 4) for k, v in per_chunk.items()},
+               "path": "tw_fused_reduce_add_rmsnorm_host: pinned host buffers, "
+                       "chunked host->device copies / kernel / device->host copies "
+                       "overlapped on three streams"}
     extra = sweep(args, None) if args.sweep and rank == 0 else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -170,6 +170,32 @@ int tw_split_launch(const void* const* partials, int n_parts,
                     float eps, int64_t t_split, int max_sms, void* s0, void* s1,
                     int dtype);
 
+/* The fused step for tensors in page-locked HOST memory (cudaHostAlloc or
+ * cudaHostRegister): partials, residual, weight, out and residual_out are host
+ * pointers with the layout and rules above; only `workspace` is device memory,
+ * at least tw_host_workspace_bytes() bytes, 256-byte aligned, owned by the
+ * caller.  Rows [t0, t1) are moved in chunks of chunk_tokens tokens: the
+ * host->device copies of one chunk, the kernel on the previous one and the
+ * device->host copies of the one before overlap on three streams the library
+ * creates once per device; `stream` orders the whole call (it waits for the
+ * last copy back).  The host buffers and the workspace are in use until the
+ * work on `stream` completes.  Returns TW_ERR_INVALID_ARG if a tensor is not
+ * page-locked host memory or the workspace is too small. */
+int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
+                                     const void* residual, const void* weight,
+                                     void* const* out, int n_out,
+                                     void* residual_out, int64_t T, int64_t H,
+                                     float eps, int64_t t0, int64_t t1,
+                                     int max_sms, void* workspace,
+                                     size_t workspace_bytes,
+                                     int64_t chunk_tokens, void* stream,
+                                     int dtype);
+
+/* Device workspace bytes tw_fused_reduce_add_rmsnorm_host needs: the weight
+ * and two slots of (n_parts + 1 + n_out + 1) chunk buffers. */
+int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H,
+                            int64_t chunk_tokens, int dtype, size_t* bytes);
+
 /* Device-side status of the calling thread's current device: nonzero when a
  * kernel gave up on a bounded wait (an async copy that never completed) since
  * the last clear.  Reading synchronises nothing; call it after the stream has

@@ -13,8 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtw.so")
-SOURCES = ["tw_api.cu", "tw_rows.cu", "tw_warp.cu", "tw_cluster.cu"]
-HEADERS = ["tw_device.cuh", "tw_internal.h"]
+SOURCES = ["tw_api.cu", "tw_rows.cu", "tw_warp.cu", "tw_cluster.cu", "tw_host.cu"]
+HEADERS = ["tw_device.cuh", "tw_internal.h", "tw_host.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

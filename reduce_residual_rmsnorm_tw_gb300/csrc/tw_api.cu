@@ -10,6 +10,7 @@
 #include <string>
 
 #include "tw.h"
+#include "tw_host.h"
 #include "tw_internal.h"
 
 namespace tw {
@@ -293,6 +294,67 @@ int fused(const Args& a, int path, uint32_t* smid_log, void* stream) {
     return launch_range(a, *d, a.t0, a.t1, path, smid_log, stream);
 }
 
+bool is_pinned_host(const void* p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return attr.type == cudaMemoryTypeHost;
+}
+
+int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
+                    int64_t chunk_tokens, void* stream) {
+    int rc = check_args(a);
+    if (rc != TW_OK) return rc;
+    if (chunk_tokens < 1)
+        return fail(TW_ERR_INVALID_ARG, "chunk_tokens %lld < 1", (long long)chunk_tokens);
+    const int64_t rb = a.H * static_cast<int64_t>(elem_size(a.dtype));
+    const size_t need = host_workspace_bytes(a.n_parts, a.n_out, rb, chunk_tokens);
+    if (!workspace) return fail(TW_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(TW_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (workspace_bytes < need)
+        return fail(TW_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need);
+    if (a.t0 == a.t1) return TW_OK;
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != TW_OK) return rc;
+    // Every tensor must be page-locked host memory (the copies are async).
+    const void* host_ptrs[TW_MAX_PARTS + TW_MAX_OUTS + 3];
+    int n_ptrs = 0;
+    for (int r = 0; r < a.n_parts; ++r) host_ptrs[n_ptrs++] = a.partials[r];
+    for (int k = 0; k < a.n_out; ++k) host_ptrs[n_ptrs++] = a.out[k];
+    host_ptrs[n_ptrs++] = a.residual;
+    host_ptrs[n_ptrs++] = a.weight;
+    host_ptrs[n_ptrs++] = a.residual_out;
+    for (int i = 0; i < n_ptrs; ++i)
+        if (!is_pinned_host(host_ptrs[i]))
+            return fail(TW_ERR_INVALID_ARG, "tensor %d is not page-locked host memory", i);
+
+    const HostCall hc{a.partials, a.n_parts, a.residual, a.weight, a.out, a.n_out,
+                      a.residual_out, rb, a.t0, a.t1, chunk_tokens, workspace, stream};
+    const DeviceState& dev = *d;
+    const LaunchChunk launch = [&](const void* const* parts, const void* residual,
+                                   const void* weight, void* const* out, void* residual_out,
+                                   int64_t n, cudaStream_t s) {
+        Args c = a;
+        c.partials = parts;
+        c.residual = residual;
+        c.weight = weight;
+        c.out = out;
+        c.residual_out = residual_out;
+        c.T = n;
+        c.t0 = 0;
+        c.t1 = n;
+        return launch_range(c, dev, 0, n, TW_PATH_AUTO, nullptr, s);
+    };
+    const char* what = nullptr;
+    rc = host_pipeline(hc, launch, &what);
+    if (rc > 0) return cuda_fail(static_cast<cudaError_t>(rc), what);
+    return rc;
+}
+
 }  // namespace
 }  // namespace tw
 
@@ -381,6 +443,27 @@ int tw_split_launch(const void* const* partials, int n_parts, const void* residu
         (e = cudaStreamWaitEvent(st0, d->join, 0)) != cudaSuccess)
         return tw::cuda_fail(e, "join");
     return TW_OK;
+}
+
+int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H, int64_t chunk_tokens, int dtype,
+                            size_t* bytes) {
+    if (!bytes || n_parts < 1 || n_parts > TW_MAX_PARTS || n_out < 1 || n_out > TW_MAX_OUTS ||
+        H < 1 || chunk_tokens < 1 || (dtype != TW_BF16 && dtype != TW_F32))
+        return tw::fail(TW_ERR_INVALID_ARG, "invalid workspace query");
+    *bytes = tw::host_workspace_bytes(n_parts, n_out, H * static_cast<int64_t>(tw::elem_size(dtype)),
+                                      chunk_tokens);
+    return TW_OK;
+}
+
+int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
+                                     const void* residual, const void* weight, void* const* out,
+                                     int n_out, void* residual_out, int64_t T, int64_t H,
+                                     float eps, int64_t t0, int64_t t1, int max_sms,
+                                     void* workspace, size_t workspace_bytes,
+                                     int64_t chunk_tokens, void* stream, int dtype) {
+    const Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+                 T,        H,       eps,      t0,     t1,  max_sms, dtype};
+    return tw::fused_from_host(a, workspace, workspace_bytes, chunk_tokens, stream);
 }
 
 int tw_device_status(int clear) {

@@ -61,6 +61,13 @@ def load():
                                     vp, i64, i64, ctypes.c_float, i64,
                                     ctypes.c_int, vp, vp, ctypes.c_int]
     lib.tw_split_launch.restype = ctypes.c_int
+    lib.tw_fused_reduce_add_rmsnorm_host.argtypes = [
+        pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64, ctypes.c_float,
+        i64, i64, ctypes.c_int, vp, ctypes.c_size_t, i64, vp, ctypes.c_int]
+    lib.tw_fused_reduce_add_rmsnorm_host.restype = ctypes.c_int
+    lib.tw_host_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64,
+                                            ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    lib.tw_host_workspace_bytes.restype = ctypes.c_int
     lib.tw_device_status.argtypes = [ctypes.c_int]
     lib.tw_device_status.restype = ctypes.c_int
     lib.tw_last_error_string.argtypes = []
@@ -189,6 +196,31 @@ def tw_split_launch(partials, residual, weight, out, residual_out, eps,
         residual_out.data_ptr(), T, H, eps, t_split,
         _ALL_SMS if max_sms is None else max_sms, _stream_handle(s0),
         _stream_handle(s1), dt)
+    _check(rc)
+
+
+def tw_host_workspace_bytes(n_parts, n_out, H, chunk_tokens, dtype):
+    """Device workspace bytes of tw_fused_reduce_add_rmsnorm_host."""
+    out = ctypes.c_size_t()
+    _check(load().tw_host_workspace_bytes(n_parts, n_out, H, chunk_tokens,
+                                          _DTYPES[dtype], ctypes.byref(out)))
+    return out.value
+
+
+def tw_fused_reduce_add_rmsnorm_host(partials, residual, weight, out,
+                                     residual_out, eps, workspace, chunk_tokens,
+                                     t0=0, t1=None, max_sms=None, stream=None):
+    """The fused step on pinned HOST tensors, pipelined in chunks of
+    ``chunk_tokens`` tokens through the device ``workspace`` (a uint8 CUDA
+    tensor of at least tw_host_workspace_bytes bytes)."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    rc = load().tw_fused_reduce_add_rmsnorm_host(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+        _ALL_SMS if max_sms is None else max_sms, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), chunk_tokens,
+        _stream_handle(stream), dt)
     _check(rc)
 
 

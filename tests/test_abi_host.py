@@ -149,3 +149,26 @@ def test_colsplit_slice_alignment(lib):
     assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 3, *args, 0, 4, 8, None, 0) == ALIGN
     assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 2, *args, 2, 2, 8, None, 0) == OK
     assert lib.tw_fused_reduce_add_rmsnorm_colsplit(p_arr, 2, *args, 0, 4, 8, None, 7) == INVALID
+
+
+def test_host_entry_workspace_and_argument_checks(lib):
+    need = tw.tw_host_workspace_bytes(8, 1, 8192, 128, torch_bf16())
+    row = 8192 * 2
+    chunk = 128 * row
+    assert need == row + 2 * (8 + 1 + 1 + 1) * chunk
+    p_arr = (ctypes.c_void_p * 2)(BASE, BASE + MB)
+    o_arr = (ctypes.c_void_p * 1)(BASE + 32 * MB)
+    args = [p_arr, 2, BASE + 64 * MB, BASE + 65 * MB, o_arr, 1, BASE + 66 * MB, 4, 64, 1e-6]
+    ws = BASE + 128 * MB
+    big = 1 << 30
+    f = lib.tw_fused_reduce_add_rmsnorm_host
+    assert f(*args, 0, 4, 8, ws, big, 0, None, 0) == INVALID        # chunk_tokens 0
+    assert f(*args, 0, 4, 8, None, big, 2, None, 0) == INVALID      # no workspace
+    assert f(*args, 0, 4, 8, ws + 16, big, 2, None, 0) == ALIGN     # workspace alignment
+    assert f(*args, 0, 4, 8, ws, 100, 2, None, 0) == INVALID        # workspace too small
+    assert f(*args, 2, 2, 8, ws, big, 2, None, 0) == OK             # empty range: no-op
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16

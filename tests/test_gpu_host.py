@@ -1,0 +1,73 @@
+"""The host-buffer entry point: pinned host tensors, a device workspace, the
+token range pipelined in chunks.  Checked against the oracle element by
+element, and bit for bit against the device entry point when every chunk
+runs on the same kernel."""
+import pytest
+import torch
+
+import oracle
+from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+from reduce_residual_rmsnorm_tw_gb300.inputs import Workload
+from tests.parity import SENTINEL, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+def host_run(wl, chunk, t0=0, t1=None):
+    t1 = wl.T if t1 is None else t1
+    d = inputs.make_inputs(wl)
+    pin = {"partials": [p.pin_memory() for p in d["partials"]],
+           "residual": d["residual"].pin_memory(), "weight": d["weight"].pin_memory()}
+    out = [torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
+           for _ in range(wl.n_out)]
+    res_out = torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
+    nbytes = tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk, wl.torch_dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    tw.tw_fused_reduce_add_rmsnorm_host(pin["partials"], pin["residual"], pin["weight"], out,
+                                        res_out, wl.eps, ws, chunk, t0, t1)
+    torch.cuda.synchronize()
+    return d, out, res_out
+
+
+CASES = [
+    Workload("host_tp8_t70_h8192_bf16", 8, 70, 8192, "bf16", 1e-5, 1, 21),
+    Workload("host_tp4_t45_h5120_f32_out4", 4, 45, 5120, "f32", 1e-6, 4, 22,
+             column_split=True),
+]
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 33, 64, 1000])
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_host_parity(wl, chunk):
+    t0, t1 = 2, wl.T - 3
+    d, out, res_out = host_run(wl, chunk, t0, t1)
+    ref_out, ref_res = oracle.reordered([inputs.to_f64(p) for p in d["partials"]],
+                                        inputs.to_f64(d["residual"]), inputs.to_f64(d["weight"]),
+                                        wl.eps, n_out=wl.n_out, t0=t0, t1=t1)
+    for k in range(wl.n_out):
+        check_close(out[k][t0:t1], ref_out[k][t0:t1], wl.dtype, f"{wl.name} out[{k}]")
+        assert bool((torch.cat([out[k][:t0], out[k][t1:]]).float() == SENTINEL).all())
+    check_close(res_out[t0:t1], ref_res[t0:t1], wl.dtype, f"{wl.name} residual_out")
+    assert bool((torch.cat([res_out[:t0], res_out[t1:]]).float() == SENTINEL).all())
+
+
+def test_host_matches_device_path_bitwise():
+    wl = CASES[0]
+    d, out, res_out = host_run(wl, 35)   # chunks of 35 tokens: the rows kernel
+    dev_out = [torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")]
+    dev_res = torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")
+    tw.tw_fused_reduce_add_rmsnorm_ex([p.cuda() for p in d["partials"]], d["residual"].cuda(),
+                                      d["weight"].cuda(), dev_out, dev_res, wl.eps, path="rows")
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], dev_out[0].cpu()) and torch.equal(res_out, dev_res.cpu())
+
+
+def test_host_rejects_pageable_memory():
+    wl = CASES[0].with_tokens(4)
+    d = inputs.make_inputs(wl)
+    out = [torch.empty(4, wl.H, dtype=wl.torch_dtype)]
+    ws = torch.empty(tw.tw_host_workspace_bytes(8, 1, wl.H, 4, wl.torch_dtype),
+                     dtype=torch.uint8, device="cuda")
+    with pytest.raises(tw.TwError, match="page-locked"):
+        tw.tw_fused_reduce_add_rmsnorm_host(d["partials"], d["residual"], d["weight"], out,
+                                            torch.empty_like(out[0]), wl.eps, ws, 4)

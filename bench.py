@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["tw", "reference"], default="tw")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="add the GEMM / fused-kernel overlap measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -407,6 +409,123 @@ def sweep(args, sync_ranks):
     return out
 
 
+# --------------------------------------------------------------- overlap ---
+def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
+    """The pages' overlap claim on one GPU ("Der intelligente Split", "Der
+    Fused Kernel"): a compute-bound bf16 GEMM (torch.matmul, cuBLAS) on one
+    stream while the fused kernel, held to a few SMs, runs on a second,
+    higher-priority stream.  Reports the GEMM's slowdown and the fused
+    kernel's throughput alone and under overlap, and a two-chunk layer step
+    (GEMM(A); GEMM(B) beside fused(A); fused(B)) against the sequential order
+    (GEMM(A+B); fused(A+B)), the GEMM writing partial 0 of each chunk."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    W = inputs.WORKLOADS
+    peak, _ = measured_peaks()
+    res = Resident(W[HEADLINE])
+    wl = res.wl
+    M = N_ = K = 8192
+    a = torch.randn(M, K, device="cuda", dtype=torch.bfloat16)
+    b = torch.randn(K, N_, device="cuda", dtype=torch.bfloat16)
+    c = torch.empty(M, N_, device="cuda", dtype=torch.bfloat16)
+    g = torch.cuda.Stream()
+    f = torch.cuda.Stream(priority=-1)
+    torch.cuda.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def gemms(n):
+        with torch.cuda.stream(g):
+            for _ in range(n):
+                torch.matmul(a, b, out=c)
+
+    gemms(3)
+    e0, e1 = ev(), ev()
+    e0.record(g)
+    gemms(gemm_reps)
+    e1.record(g)
+    torch.cuda.synchronize()
+    gemm_ms = e0.elapsed_time(e1) / gemm_reps
+    out = {"gemm": {"shape": [M, N_, K], "ms": round(gemm_ms, 4),
+                    "tflops": round(2 * M * N_ * K / (gemm_ms * 1e-3) / 1e12, 1)}}
+    bytes_launch = wl.bytes_per_token() * wl.T
+    for bud in budgets:
+        launchers = res.launchers(max_sms=bud)
+        alone = device_leg(res, 10, 3, max_sms=bud)["mean_launch_ms"]
+        n_fused = max(2, int(gemm_reps * gemm_ms / alone))
+        gemms(2)
+        g0, g1, f0, f1 = ev(), ev(), ev(), ev()
+        g0.record(g)
+        gemms(gemm_reps)
+        g1.record(g)
+        f0.record(f)
+        for i in range(n_fused):
+            launchers[i % len(launchers)](f.cuda_stream)
+        f1.record(f)
+        torch.cuda.synchronize()
+        gemm_ov = g0.elapsed_time(g1) / gemm_reps
+        fused_ov = f0.elapsed_time(f1) / n_fused
+        out[str(bud)] = {
+            "fused_alone_us": round(alone * 1e3, 1), "fused_overlap_us": round(fused_ov * 1e3, 1),
+            "fused_overlap_gbs": round(bytes_launch / (fused_ov * 1e-3) / 1e9, 1),
+            "gemm_overlap_ms": round(gemm_ov, 4), "gemm_slowdown": round(gemm_ov / gemm_ms, 4)}
+    check_status()
+    del res, a, b, c
+    torch.cuda.empty_cache()
+
+    # Two-chunk layer step on the 16384-token batch: the GEMM of each chunk
+    # writes that chunk's rows of partial 0, the fused step reads them.
+    wl = W["split_tp8_t16384_h8192_bf16"]
+    d = inputs.make_inputs(wl, device="cuda")
+    o = [torch.empty_like(d["residual"])]
+    ro = torch.empty_like(d["residual"])
+    x = torch.randn(wl.T, 8192, device="cuda", dtype=torch.bfloat16)
+    wmat = torch.randn(8192, wl.H, device="cuda", dtype=torch.bfloat16) * 0.01
+    half = wl.T // 2
+    torch.cuda.synchronize()
+
+    def fused(t0, t1, budget, stream):
+        tw.tw_fused_reduce_add_rmsnorm(d["partials"], d["residual"], d["weight"], o, ro,
+                                       wl.eps, t0, t1, max_sms=budget, stream=stream)
+
+    def sequential():
+        with torch.cuda.stream(g):
+            torch.matmul(x, wmat, out=d["partials"][0])
+            fused(0, wl.T, None, g)
+
+    def two_chunk(budget):
+        done_a, done_b = torch.cuda.Event(), torch.cuda.Event()
+        with torch.cuda.stream(g):
+            torch.matmul(x[:half], wmat, out=d["partials"][0][:half])
+            done_a.record(g)
+            torch.matmul(x[half:], wmat, out=d["partials"][0][half:])
+            done_b.record(g)
+        f.wait_event(done_a)
+        fused(0, half, budget, f)
+        f.wait_event(done_b)
+        fused(half, wl.T, None, f)
+        g.wait_stream(f)
+
+    def timed(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        s0, s1 = ev(), ev()
+        s0.record(g)
+        for _ in range(reps):
+            fn()
+        s1.record(g)
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / reps
+
+    layer = {"sequential_ms": round(timed(sequential), 4)}
+    for bud in (8, 16, 32, 48, 64):
+        layer[f"two_chunk_budget_{bud}_ms"] = round(timed(lambda: two_chunk(bud)), 4)
+    check_status()
+    out["layer_step_t16384"] = layer
+    return out
+
+
 # ------------------------------------------------------------------ main ---
 def max_over_ranks(values, world):
     """Element-wise max of a list of floats over all ranks (host-side gloo
@@ -477,6 +596,7 @@ def tw_main(args):
                        "chunked host->device copies / kernel / device->host copies "
                        "overlapped on three streams"}
     extra = sweep(args, None) if args.sweep and rank == 0 else None
+    overlap = overlap_leg() if args.overlap and rank == 0 else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
@@ -505,6 +625,8 @@ def tw_main(args):
     }
     if extra is not None:
         line["sweep"] = extra
+    if overlap is not None:
+        line["overlap"] = overlap
     print(json.dumps(line))
     return 0
 

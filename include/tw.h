@@ -75,8 +75,9 @@ extern "C" {
 
 #define TW_MAX_PARTS 16
 #define TW_MAX_OUTS 8
-/* Largest hidden size: 16384 bf16 or 8192 fp32 features (the row kernel keeps
- * one token's fp32 x in registers, 64 floats per thread over 256 threads). */
+/* Largest hidden size: 16384 bf16 or 8192 fp32 features, 32 KB per row (the
+ * rows kernel keeps one token's fp32 x in registers, 32 floats per thread over
+ * 512 threads). */
 #define TW_MAX_H_BF16 16384
 #define TW_MAX_H_F32 8192
 

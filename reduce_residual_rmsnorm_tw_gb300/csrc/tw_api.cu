@@ -214,7 +214,6 @@ Params make_params(const Args& a, const DeviceState& d, int64_t t0, int64_t t1,
     p.row_bytes = a.H * static_cast<int64_t>(elem_size(a.dtype));
     p.n_parts = a.n_parts;
     p.n_out = a.n_out;
-    p.n_chunks = static_cast<int>((p.row_bytes + kChunkBytes - 1) / kChunkBytes);
     p.colsplit = a.colsplit;
     const int64_t es = static_cast<int64_t>(elem_size(a.dtype));
     for (int r = 0; r <= a.n_parts; ++r) p.col_lo[r] = (a.H * r / a.n_parts) * es;
@@ -250,15 +249,22 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 
     int err;
     if (path == TW_PATH_ROWS) {
+        // Whole input rows per stage: as many as fit kStageTargetBytes (at
+        // least one), and as many stages as fit the shared memory.
         const int staged = rows_staged_rows(a.n_parts, a.colsplit);
-        const size_t stage = static_cast<size_t>(staged) * kChunkBytes;
+        int64_t per_stage = kStageTargetBytes / p.row_bytes;
+        if (per_stage < 1) per_stage = 1;
+        if (per_stage > staged) per_stage = staged;
+        p.rows_per_stage = static_cast<int>(per_stage);
+        const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);
         int stages = static_cast<int>(
-            (static_cast<size_t>(d.smem_optin) - rows_smem_bytes(staged, 0)) / stage);
+            (static_cast<size_t>(d.smem_optin) - rows_smem_bytes(0, 0)) / stage);
         if (stages > kMaxStages) stages = kMaxStages;
         if (stages < kMinStages)
-            return fail(TW_ERR_UNSUPPORTED, "shared memory too small for %d partials", a.n_parts);
+            return fail(TW_ERR_UNSUPPORTED, "shared memory too small for rows of %lld bytes",
+                        (long long)p.row_bytes);
         p.stages = stages;
-        size_t smem = rows_smem_bytes(staged, stages);
+        size_t smem = rows_smem_bytes(stage, stages);
         if (smem < static_cast<size_t>(kExclusiveSmemBytes)) smem = kExclusiveSmemBytes;
         const int grid = static_cast<int>(tokens < sms ? tokens : sms);
         err = launch_rows(p, a.dtype, grid, smem, pdl, stream);

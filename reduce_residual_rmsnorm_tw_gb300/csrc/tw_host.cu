@@ -1,12 +1,13 @@
 // tw_host.cu -- the fused step for tensors that live in pinned HOST memory.
 //
 // The token range is cut into chunks of `chunk_tokens` tokens that flow
-// through two slots of a caller-provided device workspace on three streams the
-// library owns per device: the host->device copies of chunk i + 1, the kernel
-// on chunk i and the device->host copies of chunk i - 1 overlap (the copy
-// engines run both directions of the host link at once).  Events order the
-// slots; the caller's stream waits for the last copy, so the call behaves like
-// one asynchronous operation on that stream.
+// through two slots of a caller-provided device workspace on streams the
+// library owns per device: the host->device copies of chunk i + 1 (spread over
+// kH2DStreams streams, so several copy engines pull at once), the kernel on
+// chunk i and the device->host copies of chunk i - 1 overlap (the copy engines
+// run both directions of the host link at once).  Events order the slots; the
+// caller's stream waits for the last copy, so the call behaves like one
+// asynchronous operation on that stream.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,14 +18,15 @@ namespace tw {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kH2DStreams = 2;
 
 size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct HostPipe {
     bool ready = false;
-    cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
+    cudaStream_t h2d[kH2DStreams] = {}, compute = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
-    cudaEvent_t in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+    cudaEvent_t in_done[2][kH2DStreams] = {}, comp_done[2] = {}, out_done[2] = {};
     std::mutex mu;  // one pipeline in flight per device at enqueue time
 };
 
@@ -38,14 +40,20 @@ cudaError_t pipe_for_device(int dev, HostPipe** out) {
     std::lock_guard<std::mutex> lock(g_pipe_init_mu);
     if (!hp.ready) {
         cudaError_t e;
-        for (cudaStream_t* s : {&hp.h2d, &hp.compute, &hp.d2h})
+        for (int i = 0; i < kH2DStreams; ++i)
+            if ((e = cudaStreamCreateWithFlags(&hp.h2d[i], cudaStreamNonBlocking)) != cudaSuccess)
+                return e;
+        for (cudaStream_t* s : {&hp.compute, &hp.d2h})
             if ((e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        cudaEvent_t* evs[] = {&hp.start, &hp.end, &hp.in_done[0], &hp.in_done[1],
-                              &hp.comp_done[0], &hp.comp_done[1], &hp.out_done[0],
-                              &hp.out_done[1]};
-        for (cudaEvent_t* ev : evs)
+        for (cudaEvent_t* ev : {&hp.start, &hp.end, &hp.comp_done[0], &hp.comp_done[1],
+                                &hp.out_done[0], &hp.out_done[1]})
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
                 return e;
+        for (int slot = 0; slot < 2; ++slot)
+            for (int i = 0; i < kH2DStreams; ++i)
+                if ((e = cudaEventCreateWithFlags(&hp.in_done[slot][i], cudaEventDisableTiming)) !=
+                    cudaSuccess)
+                    return e;
         hp.ready = true;
     }
     *out = &hp;
@@ -90,9 +98,11 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
     } while (0)
 
     TW_TRY(cudaEventRecord(hp->start, user), "cudaEventRecord");
-    for (cudaStream_t s : {hp->h2d, hp->compute, hp->d2h})
+    for (int i = 0; i < kH2DStreams; ++i)
+        TW_TRY(cudaStreamWaitEvent(hp->h2d[i], hp->start, 0), "cudaStreamWaitEvent");
+    for (cudaStream_t s : {hp->compute, hp->d2h})
         TW_TRY(cudaStreamWaitEvent(s, hp->start, 0), "cudaStreamWaitEvent");
-    TW_TRY(cudaMemcpyAsync(d_weight, c.weight, rb, cudaMemcpyHostToDevice, hp->h2d),
+    TW_TRY(cudaMemcpyAsync(d_weight, c.weight, rb, cudaMemcpyHostToDevice, hp->h2d[0]),
            "cudaMemcpyAsync");
 
     const int64_t n_chunks = (c.t1 - c.t0 + c.chunk_tokens - 1) / c.chunk_tokens;
@@ -103,19 +113,22 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
         const size_t bytes = static_cast<size_t>(n) * rb;
         const size_t host_off = static_cast<size_t>(first) * rb;
         // The slot's previous chunk must be summed and copied back first.
-        if (i >= 2) TW_TRY(cudaStreamWaitEvent(hp->h2d, hp->out_done[slot], 0), "wait slot");
-        for (int r = 0; r < c.n_parts; ++r)
-            TW_TRY(cudaMemcpyAsync(in_buf(slot, r),
-                                   static_cast<const char*>(c.partials[r]) + host_off, bytes,
-                                   cudaMemcpyHostToDevice, hp->h2d),
+        if (i >= 2)
+            for (int j = 0; j < kH2DStreams; ++j)
+                TW_TRY(cudaStreamWaitEvent(hp->h2d[j], hp->out_done[slot], 0), "wait slot");
+        // Input rows r = 0..n_parts (the residual last) alternate over the
+        // host->device streams.
+        for (int r = 0; r <= c.n_parts; ++r) {
+            const void* src = r < c.n_parts ? c.partials[r] : c.residual;
+            TW_TRY(cudaMemcpyAsync(in_buf(slot, r), static_cast<const char*>(src) + host_off,
+                                   bytes, cudaMemcpyHostToDevice, hp->h2d[r % kH2DStreams]),
                    "cudaMemcpyAsync");
-        TW_TRY(cudaMemcpyAsync(in_buf(slot, c.n_parts),
-                               static_cast<const char*>(c.residual) + host_off, bytes,
-                               cudaMemcpyHostToDevice, hp->h2d),
-               "cudaMemcpyAsync");
-        TW_TRY(cudaEventRecord(hp->in_done[slot], hp->h2d), "cudaEventRecord");
-
-        TW_TRY(cudaStreamWaitEvent(hp->compute, hp->in_done[slot], 0), "cudaStreamWaitEvent");
+        }
+        for (int j = 0; j < kH2DStreams; ++j) {
+            TW_TRY(cudaEventRecord(hp->in_done[slot][j], hp->h2d[j]), "cudaEventRecord");
+            TW_TRY(cudaStreamWaitEvent(hp->compute, hp->in_done[slot][j], 0),
+                   "cudaStreamWaitEvent");
+        }
         const void* d_parts[TW_MAX_PARTS];
         void* d_outs[TW_MAX_OUTS];
         for (int r = 0; r < c.n_parts; ++r) d_parts[r] = in_buf(slot, r);
@@ -135,8 +148,8 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
                "cudaMemcpyAsync");
         TW_TRY(cudaEventRecord(hp->out_done[slot], hp->d2h), "cudaEventRecord");
     }
-    // The caller's stream continues after the last copy back; the other two
-    // streams' work precedes it through the events.
+    // The caller's stream continues after the last copy back; the copies in
+    // and the kernels precede it through the events.
     TW_TRY(cudaEventRecord(hp->end, hp->d2h), "cudaEventRecord");
     TW_TRY(cudaStreamWaitEvent(user, hp->end, 0), "cudaStreamWaitEvent");
 #undef TW_TRY

@@ -7,14 +7,14 @@
 
 namespace tw {
 
-// Consumer threads of the rows kernel: one 16-byte vector per thread per
-// staged chunk, so a chunk row is kRowsThreads * 16 bytes.
-constexpr int kRowsThreads = 256;
-constexpr int kChunkBytes = kRowsThreads * 16;
-// Consumer groups of the rows kernel: group g sums the chunks c = g mod kRowsGroups.
-constexpr int kRowsGroups = 2;
-// Chunks per token the rows kernel keeps in registers (H <= 8 * 4 KB bytes).
-constexpr int kMaxChunks = 8;
+// Consumer threads of the rows kernel; thread i owns the 16-byte vectors
+// i, i + kRowsThreads, ... of a token row (at most kRowsMaxVecs of them, so a
+// row is at most kRowsThreads * kRowsMaxVecs * 16 = 32 KB).
+constexpr int kRowsThreads = 512;
+constexpr int kRowsMaxVecs = 4;
+// Target bytes of one ring stage: whole input rows of one token are staged,
+// as many as fit this size (at least one).
+constexpr int kStageTargetBytes = 48 * 1024;
 // Ring depth bounds of the rows kernel.
 constexpr int kMaxStages = 16;
 constexpr int kMinStages = 2;
@@ -45,8 +45,8 @@ struct Params {
     // staged chunk then holds the concatenation in one row.
     int64_t col_lo[TW_MAX_PARTS + 1];
     int n_parts, n_out;
-    int n_chunks;           // ceil(row_bytes / kChunkBytes), rows kernel
-    int stages;             // ring depth, rows kernel
+    int rows_per_stage;     // rows kernel: whole input rows per ring stage
+    int stages;             // rows kernel: ring depth
     int colsplit;           // 1: column-split mode
     float eps;
     float inv_H;
@@ -60,9 +60,11 @@ int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pd
                 void* stream);
 int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream);
-// Rows staged per ring stage and shared memory of a ring depth.
+// Input rows per token the rows kernel stages (partials + residual, or the
+// assembled column-split row + residual), and its shared memory for a stage
+// size and ring depth.
 int rows_staged_rows(int n_parts, int colsplit);
-size_t rows_smem_bytes(int staged_rows, int stages);
+size_t rows_smem_bytes(size_t stage_bytes, int stages);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).
 int rows_set_smem_limit(int smem_optin);

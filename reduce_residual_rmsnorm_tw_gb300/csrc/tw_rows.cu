@@ -7,37 +7,35 @@
 //   inv = 1 / sqrt(mean_h x^2 + eps)
 //   out[k][t,h] = x * inv * weight[h]                 for every destination k
 //
-// Layout of the work: a token's R = N + 1 input rows (the N partials and the
-// residual) are cut into chunks of kChunkBytes per row.  One elected thread of
-// the producer warp streams chunks into a ring of shared-memory stages with
-// 1-D bulk async copies (cp.async.bulk, no tensor map, no multicast), each
-// stage tracked by a "full" mbarrier (transaction bytes) and an "empty"
-// mbarrier (one arrival per consuming warp).  Two consumer groups of 256
-// threads take alternate chunks of each token (group g the chunks c = g mod 2),
-// so two stages are being summed at any time.  A consumer thread owns one
-// 16-byte vector of each of its chunks: it sums the staged rows in fp32 (ranks
-// in order, residual last), stores residual_out at once, keeps x in
-// registers, and after the token's last chunk the sum of squares goes through
-// a warp shuffle and the 16 warp totals through shared memory behind one named
-// barrier; then the weighted result is stored to every gather destination.
-// The N-way sum happens while the data streams through shared memory, the
-// counterpart of the pages' sum-at-load.
+// Layout of the work: a token has R = N + 1 input rows (the N partials, then
+// the residual), each H * b contiguous bytes.  One elected thread of the
+// producer warp streams them, whole rows at a time, into a ring of
+// shared-memory stages with 1-D bulk async copies (cp.async.bulk, one copy per
+// row, no tensor map, no multicast); a stage holds `rows_per_stage` rows of
+// one token and is tracked by a "full" mbarrier (transaction bytes) and an
+// "empty" mbarrier (one arrival per consumer warp).  Whole-row copies keep
+// several large copies from different buffers in flight, which is what lets
+// one SM stream well above its share of HBM bandwidth.  The 512 consumer
+// threads own the 16-byte vectors tid, tid + 512, ... of the row: they add the
+// staged rows into fp32 registers in row order (ranks first, residual last),
+// store residual_out once the residual row is in, and after the token's last
+// stage the sum of squares goes through a warp shuffle and the 16 warp totals
+// through shared memory behind one named barrier; then the weighted result is
+// stored to every gather destination.  The N-way sum happens while the data
+// streams through shared memory, the counterpart of the pages' sum-at-load.
 //
 // Column-split mode ("TokenWeave 策略详解", appendix 实现方法：零填充 +
 // AllReduce 求和): partial r is zero outside its own column slice, so the sum
-// is the concatenation of the slices.  The producer copies only each rank's
-// slice of a chunk into one staged row; adding the zeros would change no bit
-// (0 + p = p exactly), so the result equals the dense mode's, with
+// is the concatenation of the slices.  The producer assembles one staged row
+// from each rank's slice (one copy per rank); adding the zeros would change no
+// bit (0 + p = p exactly), so the result equals the dense mode's, with
 // (1 + 1 + n_out + 1) rows of traffic per token instead of (N + 1 + n_out + 1).
 #include "tw_device.cuh"
 
 namespace tw {
 namespace {
 
-constexpr int kGroups = kRowsGroups;
-constexpr int kGroupWarps = kRowsThreads / 32;
-constexpr int kConsumerThreads = kGroups * kRowsThreads;
-constexpr int kConsumerWarps = kConsumerThreads / 32;
+constexpr int kConsumerWarps = kRowsThreads / 32;
 constexpr int kFullOff = 0;
 constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
@@ -61,21 +59,23 @@ struct RingPos {
     }
 };
 
-template <typename T, int NC>
-__global__ void __launch_bounds__(kConsumerThreads + 32, 1)
+template <typename T, int NV>
+__global__ void __launch_bounds__(kRowsThreads + 32, 1)
     rows_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     using V = Vec<T>;
     constexpr int E = V::kElems;
-    constexpr int kSlots = (NC + kGroups - 1) / kGroups;  // chunks per thread and token
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const int n_sum = p.colsplit ? 1 : p.n_parts;  // staged rows summed before the residual
-    const int R = n_sum + 1;
-    const uint32_t stage_bytes = static_cast<uint32_t>(R) * kChunkBytes;
+    const int R = n_sum + 1;                        // staged rows per token
+    const int G = p.rows_per_stage;
+    const int stages_per_token = (R + G - 1) / G;
+    const int64_t rb = p.row_bytes;
+    const uint32_t stage_bytes = static_cast<uint32_t>(G * rb);
     const uint32_t full0 = smem_addr(smem + kFullOff);
     const uint32_t empty0 = smem_addr(smem + kEmptyOff);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
     if (tid == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kGroupWarps);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
 
     const int64_t first = p.t0 + blockIdx.x;
     const int64_t stride = gridDim.x;
-    const int64_t rb = p.row_bytes;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer ---
@@ -110,7 +109,8 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
         uint32_t issued = 0;
         bool stop = false;
         for (int64_t t = first; t < p.t1 && !stop; t += stride) {
-            for (int c = 0; c < NC; ++c, ++issued, pos.advance(S)) {
+            const int64_t row_off = t * rb;
+            for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
                 const uint32_t s = pos.stage;
                 if (*abort_flag ||
                     (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag))) {
@@ -118,33 +118,29 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
                     stop = true;
                     break;
                 }
-                const int64_t off = static_cast<int64_t>(c) * kChunkBytes;
-                const int64_t left = rb - off;
-                const uint32_t bytes = left < kChunkBytes ? static_cast<uint32_t>(left)
-                                                          : static_cast<uint32_t>(kChunkBytes);
+                const int g0 = k * G;
+                const int g1 = g0 + G < R ? g0 + G : R;
                 const uint32_t bar = full0 + 8 * s;
-                mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(R));
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>((g1 - g0) * rb));
                 uint32_t dst = ring_addr + s * stage_bytes;
-                const int64_t src_off = t * rb + off;
-                if (p.colsplit) {
-                    // Row 0 of the stage receives, from each rank, the part of
-                    // its column slice that falls in this chunk.
-                    for (int r = 0; r < p.n_parts; ++r) {
-                        const int64_t lo = p.col_lo[r] > off ? p.col_lo[r] : off;
-                        const int64_t end = off + bytes;
-                        const int64_t hi = p.col_lo[r + 1] < end ? p.col_lo[r + 1] : end;
-                        if (lo < hi)
-                            bulk_g2s(dst + static_cast<uint32_t>(lo - off),
-                                     static_cast<const char*>(p.partials[r]) + t * rb + lo,
-                                     static_cast<uint32_t>(hi - lo), bar, pol);
+                for (int g = g0; g < g1; ++g, dst += static_cast<uint32_t>(rb)) {
+                    if (g == n_sum) {
+                        bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off,
+                                 static_cast<uint32_t>(rb), bar, pol);
+                    } else if (p.colsplit) {
+                        // One staged row from every rank's own column slice.
+                        for (int r = 0; r < p.n_parts; ++r) {
+                            const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
+                            if (lo < hi)
+                                bulk_g2s(dst + static_cast<uint32_t>(lo),
+                                         static_cast<const char*>(p.partials[r]) + row_off + lo,
+                                         static_cast<uint32_t>(hi - lo), bar, pol);
+                        }
+                    } else {
+                        bulk_g2s(dst, static_cast<const char*>(p.partials[g]) + row_off,
+                                 static_cast<uint32_t>(rb), bar, pol);
                     }
-                    dst += kChunkBytes;
-                } else {
-                    for (int r = 0; r < p.n_parts; ++r, dst += kChunkBytes)
-                        bulk_g2s(dst, static_cast<const char*>(p.partials[r]) + src_off, bytes,
-                                 bar, pol);
                 }
-                bulk_g2s(dst, static_cast<const char*>(p.residual) + src_off, bytes, bar, pol);
             }
         }
         // Drain: the copies of the last S issued stages must have landed before
@@ -164,58 +160,61 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
     }
 
     // ---------------------------------------------------------- consumers ---
-    const int group = warp / kGroupWarps;       // consumes chunks c with c % kGroups == group
-    const int gtid = tid - group * kRowsThreads;  // 0 .. kRowsThreads-1 within the group
     const int64_t nvec = rb / 16;
-    uint4 wv[kSlots];
+    uint4 wv[NV];
 #pragma unroll
-    for (int j = 0; j < kSlots; ++j) {
-        const int c = group + j * kGroups;
-        const int64_t v = static_cast<int64_t>(c) * kRowsThreads + gtid;
-        wv[j] = (c < NC && v < nvec) ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
-                                     : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < NV; ++j) {
+        const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
+        wv[j] = v < nvec ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
+                         : make_uint4(0, 0, 0, 0);
     }
 
     RingPos pos;
     int red_buf = 0;
     bool alive = true;
     for (int64_t t = first; t < p.t1; t += stride) {
-        float x[kSlots][E];
+        float x[NV][E];
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[j][e] = 0.f;
+        for (int k = 0; k < stages_per_token; ++k, pos.advance(S)) {
+            const uint32_t s = pos.stage;
+            if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
+                give_up(p, abort_flag);
+                alive = false;
+            }
+            const int g0 = k * G;
+            const int g1 = g0 + G < R ? g0 + G : R;
+            const unsigned char* stage = ring + s * stage_bytes + tid * 16;
+            for (int g = g0; g < g1; ++g) {
+                const unsigned char* row = stage + (g - g0) * rb;
+#pragma unroll
+                for (int j = 0; j < NV; ++j)
+                    if (static_cast<int64_t>(j) * kRowsThreads + tid < nvec)
+                        add_vec(x[j],
+                                *reinterpret_cast<const uint4*>(row + j * kRowsThreads * 16),
+                                static_cast<T*>(nullptr));
+            }
+            __syncwarp();
+            if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // The residual (the last staged row) is in: store residual_out and
+        // reduce the sum of squares over the token.
         float ss2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            if (c % kGroups == group) {
-                const int j = c / kGroups;
-                const uint32_t s = pos.stage;
-                if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
-                    give_up(p, abort_flag);
-                    alive = false;
-                }
-                const int64_t v = static_cast<int64_t>(c) * kRowsThreads + gtid;
-#pragma unroll
-                for (int e = 0; e < E; ++e) x[j][e] = 0.f;
-                if (v < nvec) {
-                    const unsigned char* src = ring + s * stage_bytes + gtid * 16;
-#pragma unroll 4
-                    for (int r = 0; r < n_sum; ++r)
-                        add_vec(x[j], *reinterpret_cast<const uint4*>(src + r * kChunkBytes),
-                                static_cast<T*>(nullptr));
-                    add_vec(x[j], *reinterpret_cast<const uint4*>(src + n_sum * kChunkBytes),
-                            static_cast<T*>(nullptr));
-                    sum_squares<E>(ss2, x[j]);
-                    if (alive)
-                        st_global_cs(static_cast<char*>(p.residual_out) + t * rb + v * 16,
-                                     V::from_float(x[j]));
-                }
-                __syncwarp();
-                if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+        for (int j = 0; j < NV; ++j) {
+            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
+            if (v < nvec) {
+                sum_squares<E>(ss2, x[j]);
+                if (alive)
+                    st_global_cs(static_cast<char*>(p.residual_out) + t * rb + v * 16,
+                                 V::from_float(x[j]));
             }
-            pos.advance(S);
         }
-        // Sum of squares over the token: warp shuffle, then the warp totals.
         const float ss = warp_sum(ss2[0] + ss2[1]);
         if (lane == 0) red[red_buf * kConsumerWarps + warp] = ss;
-        named_barrier(1, kConsumerThreads);
+        named_barrier(1, kRowsThreads);
         float total = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) total += red[red_buf * kConsumerWarps + w];
@@ -223,10 +222,9 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
         const float inv = rsqrtf(total * p.inv_H + p.eps);
 
 #pragma unroll
-        for (int j = 0; j < kSlots; ++j) {
-            const int c = group + j * kGroups;
-            const int64_t v = static_cast<int64_t>(c) * kRowsThreads + gtid;
-            if (c < NC && v < nvec && alive) {
+        for (int j = 0; j < NV; ++j) {
+            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
+            if (v < nvec && alive) {
                 float w[E], y[E];
                 V::to_float(wv[j], w);
 #pragma unroll
@@ -239,43 +237,37 @@ __global__ void __launch_bounds__(kConsumerThreads + 32, 1)
     }
 }
 
-template <typename T, int NC>
-void* rows_entry() {
-    return reinterpret_cast<void*>(&rows_kernel<T, NC>);
-}
-
 template <typename T>
-void* rows_entry_for(int nc) {
-    switch (nc) {
-        case 1: return rows_entry<T, 1>();
-        case 2: return rows_entry<T, 2>();
-        case 3: return rows_entry<T, 3>();
-        case 4: return rows_entry<T, 4>();
-        case 5: return rows_entry<T, 5>();
-        case 6: return rows_entry<T, 6>();
-        case 7: return rows_entry<T, 7>();
-        case 8: return rows_entry<T, 8>();
+void* rows_entry_for(int nv) {
+    switch (nv) {
+        case 1: return reinterpret_cast<void*>(&rows_kernel<T, 1>);
+        case 2: return reinterpret_cast<void*>(&rows_kernel<T, 2>);
+        case 3: return reinterpret_cast<void*>(&rows_kernel<T, 3>);
+        case 4: return reinterpret_cast<void*>(&rows_kernel<T, 4>);
         default: return nullptr;
     }
 }
 
-void* rows_kernel_for(int dtype, int nc) {
-    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nc) : rows_entry_for<float>(nc);
+void* rows_kernel_for(int dtype, int nv) {
+    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nv) : rows_entry_for<float>(nv);
+}
+
+int rows_vectors_per_thread(int64_t row_bytes) {
+    return static_cast<int>((row_bytes / 16 + kRowsThreads - 1) / kRowsThreads);
 }
 
 }  // namespace
 
 int rows_staged_rows(int n_parts, int colsplit) { return colsplit ? 2 : n_parts + 1; }
 
-size_t rows_smem_bytes(int staged_rows, int stages) {
-    return static_cast<size_t>(kRingOff) +
-           static_cast<size_t>(stages) * static_cast<size_t>(staged_rows) * kChunkBytes;
+size_t rows_smem_bytes(size_t stage_bytes, int stages) {
+    return static_cast<size_t>(kRingOff) + static_cast<size_t>(stages) * stage_bytes;
 }
 
 int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
-        for (int nc = 1; nc <= kMaxChunks; ++nc) {
-            cudaError_t e = cudaFuncSetAttribute(rows_kernel_for(dt, nc),
+        for (int nv = 1; nv <= kRowsMaxVecs; ++nv) {
+            cudaError_t e = cudaFuncSetAttribute(rows_kernel_for(dt, nv),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  smem_optin);
             if (e != cudaSuccess) return static_cast<int>(e);
@@ -285,9 +277,9 @@ int rows_set_smem_limit(int smem_optin) {
 
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream) {
-    void* fn = rows_kernel_for(dtype, p.n_chunks);
+    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes));
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
-    return launch_with_pdl(fn, p, grid, kConsumerThreads + 32, smem_bytes, pdl, stream);
+    return launch_with_pdl(fn, p, grid, kRowsThreads + 32, smem_bytes, pdl, stream);
 }
 
 }  // namespace tw

@@ -159,6 +159,28 @@ int tw_fused_reduce_add_rmsnorm_colsplit(const void* const* partials, int n_part
                                          float eps, int64_t t0, int64_t t1,
                                          int max_sms, void* stream, int dtype);
 
+/* Readiness flags (the FLUX notes' producer/consumer signals, WaitSignal and
+ * SetSignal): the same step, but no row of token t is read before
+ * ready[t / block_tokens] has reached `epoch` (compared as the signed 32-bit
+ * difference ready - epoch >= 0, so epochs may wrap).  `ready` is a DEVICE
+ * array of ceil(T / block_tokens) uint32 counters, 4-byte aligned, that a
+ * producer raises (with release semantics) once the block's partials and
+ * residual rows are written; it is read with acquire semantics at GPU scope.
+ * Raising the counter per step (epoch = step number) reuses the array without
+ * resetting it.  The wait is bounded: if a block's flag has not arrived
+ * within about one second, the kernel stops reading and writing, sets the
+ * value 4 in the device status word (tw_device_status) and returns; the rows
+ * of the tokens that were waiting are then left unwritten (rows written before
+ * are complete).  Runs on the rows kernel. */
+int tw_fused_reduce_add_rmsnorm_flags(const void* const* partials, int n_parts,
+                                      const void* residual, const void* weight,
+                                      void* const* out, int n_out,
+                                      void* residual_out, int64_t T, int64_t H,
+                                      float eps, int64_t t0, int64_t t1,
+                                      int max_sms, void* stream, int dtype,
+                                      const uint32_t* ready,
+                                      int64_t block_tokens, uint32_t epoch);
+
 /* Two-chunk token split ("Der intelligente Split"): rows [0, t_split) run on
  * stream s0 and rows [t_split, T) on stream s1, each a rows-kernel launch with
  * its own budget of max_sms SMs (so up to 2*max_sms SMs while both run).
@@ -198,8 +220,9 @@ int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H,
                             int64_t chunk_tokens, int dtype, size_t* bytes);
 
 /* Device-side status of the calling thread's current device: nonzero when a
- * kernel gave up on a bounded wait (an async copy that never completed) since
- * the last clear.  Reading synchronises nothing; call it after the stream has
+ * kernel gave up on a bounded wait since the last clear, as an OR of 1 (an
+ * async copy or stage that never completed), 2 (copies still in flight at
+ * exit) and 4 (a readiness flag that never arrived).  Reading synchronises nothing; call it after the stream has
  * finished.  clear != 0 resets the word.  Returns -1 on a CUDA error. */
 int tw_device_status(int clear);
 

@@ -117,6 +117,9 @@ struct Args {
     int max_sms;
     int dtype;
     int colsplit = 0;
+    const unsigned int* ready = nullptr;  // readiness flags (rows kernel only)
+    int64_t block_tokens = 0;
+    unsigned int epoch = 0;
 };
 
 size_t elem_size(int dtype) { return dtype == TW_BF16 ? 2 : 4; }
@@ -215,6 +218,9 @@ Params make_params(const Args& a, const DeviceState& d, int64_t t0, int64_t t1,
     p.n_parts = a.n_parts;
     p.n_out = a.n_out;
     p.colsplit = a.colsplit;
+    p.ready = a.ready;
+    p.block_tokens = a.block_tokens;
+    p.epoch = a.epoch;
     const int64_t es = static_cast<int64_t>(elem_size(a.dtype));
     for (int r = 0; r <= a.n_parts; ++r) p.col_lo[r] = (a.H * r / a.n_parts) * es;
     p.eps = a.eps;
@@ -237,9 +243,10 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
     while (cluster * 2 <= 8 && cluster * 2 <= sms) cluster *= 2;
     const bool cluster_ok =
         d.cluster_ready && cluster_vectors_per_thread(p.row_bytes, cluster) != 0;
-    if (a.colsplit) {
+    if (a.colsplit || a.ready) {
         if (path != TW_PATH_AUTO && path != TW_PATH_ROWS)
-            return fail(TW_ERR_UNSUPPORTED, "the column-split mode runs on the rows kernel only");
+            return fail(TW_ERR_UNSUPPORTED,
+                        "the column-split mode and readiness flags run on the rows kernel only");
         path = TW_PATH_ROWS;
     }
     if (path == TW_PATH_AUTO)
@@ -386,6 +393,26 @@ int tw_fused_reduce_add_rmsnorm_colsplit(const void* const* partials, int n_part
     Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
            T,        H,       eps,      t0,     t1,  max_sms, dtype};
     a.colsplit = 1;
+    return tw::fused(a, TW_PATH_ROWS, nullptr, stream);
+}
+
+int tw_fused_reduce_add_rmsnorm_flags(const void* const* partials, int n_parts,
+                                      const void* residual, const void* weight,
+                                      void* const* out, int n_out, void* residual_out,
+                                      int64_t T, int64_t H, float eps, int64_t t0, int64_t t1,
+                                      int max_sms, void* stream, int dtype,
+                                      const uint32_t* ready, int64_t block_tokens,
+                                      uint32_t epoch) {
+    if (!ready) return tw::fail(TW_ERR_INVALID_ARG, "ready is NULL");
+    if ((reinterpret_cast<uintptr_t>(ready) & 3u) != 0)
+        return tw::fail(TW_ERR_ALIGNMENT, "ready must be 4-byte aligned");
+    if (block_tokens < 1)
+        return tw::fail(TW_ERR_INVALID_ARG, "block_tokens %lld < 1", (long long)block_tokens);
+    Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+           T,        H,       eps,      t0,     t1,  max_sms, dtype};
+    a.ready = ready;
+    a.block_tokens = block_tokens;
+    a.epoch = epoch;
     return tw::fused(a, TW_PATH_ROWS, nullptr, stream);
 }
 

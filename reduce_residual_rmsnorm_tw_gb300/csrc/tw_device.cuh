@@ -80,6 +80,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// Wait until *flag has reached `epoch` (compared wrap-safe as a signed
+// difference), reading with acquire semantics at GPU scope, then order the
+// async proxy (bulk copies) after it.  Returns false after kWaitLimitNs or
+// when the CTA is aborting.
+__device__ __forceinline__ bool flag_wait(const unsigned int* flag, unsigned int epoch,
+                                          const volatile int* abort) {
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (static_cast<int>(v - epoch) >= 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if (abort && *abort) return false;
+        if (global_timer_ns() - start > kWaitLimitNs) return false;
+        __nanosleep(256);
+    }
+}
+
 // ------------------------------------------------------ bulk async copy ---
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

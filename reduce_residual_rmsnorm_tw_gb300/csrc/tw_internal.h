@@ -44,6 +44,11 @@ struct Params {
     // range [col_lo[r], col_lo[r + 1]) of each row, which alone is read; the
     // staged chunk then holds the concatenation in one row.
     int64_t col_lo[TW_MAX_PARTS + 1];
+    // Readiness flags (rows kernel): when `ready` is not NULL, token t is read
+    // only once ready[t / block_tokens] has reached `epoch` (wrap-safe).
+    const unsigned int* ready;
+    int64_t block_tokens;
+    unsigned int epoch;
     int n_parts, n_out;
     int rows_per_stage;     // rows kernel: whole input rows per ring stage
     int stages;             // rows kernel: ring depth

@@ -24,6 +24,11 @@
 // stored to every gather destination.  The N-way sum happens while the data
 // streams through shared memory, the counterpart of the pages' sum-at-load.
 //
+// Readiness flags (the FLUX notes' WaitSignal / SetSignal): with a `ready`
+// array, the producer reads no row of token t before ready[t / block_tokens]
+// has reached the call's epoch -- a bounded acquire wait; if a flag never
+// arrives the CTA gives up (status bit 4), writes nothing more and exits.
+//
 // Column-split mode ("TokenWeave 策略详解", appendix 实现方法：零填充 +
 // AllReduce 求和): partial r is zero outside its own column slice, so the sum
 // is the concatenation of the slices.  The producer assembles one staged row
@@ -108,8 +113,20 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
         RingPos pos;
         uint32_t issued = 0;
         bool stop = false;
+        int64_t ready_block = -1;  // last flag block seen ready
         for (int64_t t = first; t < p.t1 && !stop; t += stride) {
             const int64_t row_off = t * rb;
+            if (p.ready) {
+                const int64_t b = t / p.block_tokens;
+                if (b != ready_block) {
+                    if (!flag_wait(p.ready + b, p.epoch, abort_flag)) {
+                        give_up(p, abort_flag);
+                        atomicOr(p.status, 4u);
+                        break;
+                    }
+                    ready_block = b;
+                }
+            }
             for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
                 const uint32_t s = pos.stage;
                 if (*abort_flag ||

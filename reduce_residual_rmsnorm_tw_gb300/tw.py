@@ -57,6 +57,9 @@ def load():
         fn = getattr(lib, name)
         fn.argtypes = common + extra
         fn.restype = ctypes.c_int
+    lib.tw_fused_reduce_add_rmsnorm_flags.argtypes = common + [
+        ctypes.c_int, vp, i64, ctypes.c_uint32]
+    lib.tw_fused_reduce_add_rmsnorm_flags.restype = ctypes.c_int
     lib.tw_split_launch.argtypes = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int,
                                     vp, i64, i64, ctypes.c_float, i64,
                                     ctypes.c_int, vp, vp, ctypes.c_int]
@@ -157,6 +160,24 @@ def tw_fused_reduce_add_rmsnorm_colsplit(partials, residual, weight, out,
         p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
         residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
         _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt)
+    _check(rc)
+
+
+def tw_fused_reduce_add_rmsnorm_flags(partials, residual, weight, out,
+                                      residual_out, eps, ready, block_tokens,
+                                      epoch, t0=0, t1=None, max_sms=None,
+                                      stream=None):
+    """The fused step gated by readiness flags: token t is read only once
+    ``ready[t // block_tokens]`` (an int32 CUDA tensor) has reached ``epoch``."""
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    if ready.dtype != torch.int32 or not ready.is_cuda:
+        raise ValueError("ready must be an int32 CUDA tensor")
+    rc = load().tw_fused_reduce_add_rmsnorm_flags(
+        p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+        residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+        _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt,
+        ready.data_ptr(), block_tokens, epoch & 0xFFFFFFFF)
     _check(rc)
 
 

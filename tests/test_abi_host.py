@@ -172,3 +172,14 @@ def test_host_entry_workspace_and_argument_checks(lib):
 def torch_bf16():
     import torch
     return torch.bfloat16
+
+
+def test_flags_argument_checks(lib):
+    p_arr = (ctypes.c_void_p * 2)(BASE, BASE + MB)
+    o_arr = (ctypes.c_void_p * 1)(BASE + 32 * MB)
+    args = [p_arr, 2, BASE + 64 * MB, BASE + 65 * MB, o_arr, 1, BASE + 66 * MB, 4, 64, 1e-6,
+            0, 4, 8, None, 0]
+    f = lib.tw_fused_reduce_add_rmsnorm_flags  # signature set by the binding
+    assert f(*args, None, 1, 1) == INVALID                    # no flag array
+    assert f(*args, BASE + 2, 1, 1) == ALIGN                  # misaligned flags
+    assert f(*args, BASE + 128 * MB, 0, 1) == INVALID         # block_tokens 0

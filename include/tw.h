@@ -219,6 +219,40 @@ int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
 int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H,
                             int64_t chunk_tokens, int dtype, size_t* bytes);
 
+/* Staging bytes the no-allocation entry point holds per GPU (see below). */
+#define TW_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The host-buffer step of tw_fused_reduce_add_rmsnorm_host for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is a
+ * convenience of this library.  Some callers cannot hand in a device
+ * workspace: a host program that reaches the GPU only through this C ABI and
+ * has no CUDA allocator of its own, a process whose device memory is all
+ * reserved up front by a framework that gives out no raw buffers, or code
+ * running where cudaMalloc is not allowed.  This entry point allocates
+ * nothing: it stages the chunks in one device array of
+ * TW_NOALLOC_SCRATCH_BYTES (16 MiB) that the library declares at file scope,
+ * which every GPU that loads the library holds until the process exits.
+ * Arguments are those of tw_fused_reduce_add_rmsnorm_host without the
+ * workspace; chunk_tokens <= 0 picks the largest chunk that fits the array,
+ * and a chunk whose staging needs more than the array holds is refused with
+ * TW_ERR_UNSUPPORTED and a message naming both sizes.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the last call's contents; nothing in it needs to start at zero
+ * (each chunk's staging is written before it is read).  Calls whose work
+ * overlaps on the GPU (for instance issued on two streams without ordering
+ * between them) race on the array: order them on one stream. */
+int tw_fused_reduce_add_rmsnorm_host_noalloc(const void* const* partials,
+                                             int n_parts, const void* residual,
+                                             const void* weight,
+                                             void* const* out, int n_out,
+                                             void* residual_out, int64_t T,
+                                             int64_t H, float eps, int64_t t0,
+                                             int64_t t1, int max_sms,
+                                             int64_t chunk_tokens, void* stream,
+                                             int dtype);
+
 /* Device-side status of the calling thread's current device: nonzero when a
  * kernel gave up on a bounded wait since the last clear, as an OR of 1 (an
  * async copy or stage that never completed), 2 (copies still in flight at

@@ -369,6 +369,9 @@ int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
 }
 
 }  // namespace
+
+int set_last_error(int code, const char* message) { return fail(code, "%s", message); }
+
 }  // namespace tw
 
 using tw::Args;

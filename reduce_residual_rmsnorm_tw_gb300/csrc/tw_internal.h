@@ -57,6 +57,9 @@ struct Params {
     float inv_H;
 };
 
+// Record `message` as the calling thread's last error and return `code`.
+int set_last_error(int code, const char* message);
+
 // Launchers (return a cudaError_t value as int).  `pdl` launches with
 // programmatic stream serialization: the kernel may start while the previous
 // kernel of the stream drains, and waits (griddepcontrol.wait) before its

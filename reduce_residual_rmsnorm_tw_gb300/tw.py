@@ -245,6 +245,29 @@ def tw_fused_reduce_add_rmsnorm_host(partials, residual, weight, out,
     _check(rc)
 
 
+def tw_fused_reduce_add_rmsnorm_host_noalloc(partials, residual, weight, out,
+                                             residual_out, eps, chunk_tokens=0,
+                                             t0=0, t1=None, max_sms=None,
+                                             stream=None):
+    """The host-buffer step for callers that cannot allocate device memory:
+    pinned host tensors only; the library stages the chunks in its own
+    fixed device array (chunk_tokens <= 0: the largest chunk that fits)."""
+    lib = load()
+    fn = lib.tw_fused_reduce_add_rmsnorm_host_noalloc
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    fn.argtypes = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64,
+                   ctypes.c_float, i64, i64, ctypes.c_int, i64, vp, ctypes.c_int]
+    fn.restype = ctypes.c_int
+    p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
+                                                out, residual_out)
+    rc = fn(p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+            residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
+            _ALL_SMS if max_sms is None else max_sms, chunk_tokens,
+            _stream_handle(stream), dt)
+    _check(rc)
+
+
 def tw_device_status(clear=False):
     """Device status word: nonzero if a kernel gave up on a bounded wait."""
     rc = load().tw_device_status(1 if clear else 0)

@@ -1,0 +1,67 @@
+"""The no-allocation host-buffer entry point, for callers that cannot allocate
+device memory (a host program with no CUDA allocator of its own, device memory
+reserved up front by a framework, code where cudaMalloc is not allowed): it
+must give the same result, within the tests' tolerance, as the host-buffer
+entry point that takes a caller-allocated workspace, on two calls in a row
+(the second on different data, so stale staging from the first cannot leak
+through).  Collected last: it works in a fresh process (where its first call
+sets up the device array's address) and after every other test."""
+import pytest
+import torch
+
+from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+from reduce_residual_rmsnorm_tw_gb300.inputs import Workload
+from tests.parity import SENTINEL, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _pinned(wl):
+    d = inputs.make_inputs(wl)
+    return ([p.pin_memory() for p in d["partials"]], d["residual"].pin_memory(),
+            d["weight"].pin_memory())
+
+
+def _outputs(wl):
+    out = [torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
+           for _ in range(wl.n_out)]
+    return out, torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_no_alloc_matches_workspace_entry_on_two_calls(dtype):
+    calls = [Workload(f"noalloc_a_{dtype}", 8, 70, 8192, dtype, 1e-5, 2, 41),
+             Workload(f"noalloc_b_{dtype}", 8, 70, 8192, dtype, 1e-6, 2, 42)]
+    ranges = [(0, 70), (3, 61)]
+    for wl, (t0, t1) in zip(calls, ranges):
+        parts, res, w = _pinned(wl)
+        out, res_out = _outputs(wl)
+        tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
+                                                    t0=t0, t1=t1)
+        ref_out, ref_res = _outputs(wl)
+        chunk = 32
+        ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk,
+                                                    wl.torch_dtype),
+                         dtype=torch.uint8, device="cuda")
+        tw.tw_fused_reduce_add_rmsnorm_host(parts, res, w, ref_out, ref_res, wl.eps, ws, chunk,
+                                            t0=t0, t1=t1)
+        torch.cuda.synchronize()
+        for k in range(wl.n_out):
+            check_close(out[k][t0:t1], inputs.to_f64(ref_out[k][t0:t1]), dtype,
+                        f"{wl.name} out[{k}]")
+            assert bool((torch.cat([out[k][:t0], out[k][t1:]]).float() == SENTINEL).all())
+        check_close(res_out[t0:t1], inputs.to_f64(ref_res[t0:t1]), dtype,
+                    f"{wl.name} residual_out")
+        assert bool((torch.cat([res_out[:t0], res_out[t1:]]).float() == SENTINEL).all())
+    assert tw.tw_device_status() == 0
+
+
+def test_no_alloc_refuses_chunks_beyond_its_array():
+    wl = Workload("noalloc_big", 8, 4096, 8192, "bf16", 1e-5, 1, 43)
+    tiny = wl.with_tokens(4)
+    parts, res, w = _pinned(tiny)
+    out, res_out = _outputs(tiny)
+    # 4096-token chunks need 2 * 11 * 4096 * 16 KB of staging, far above 16 MiB.
+    with pytest.raises(tw.TwError, match="TW_ERR_UNSUPPORTED"):
+        tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
+                                                    chunk_tokens=4096)

@@ -161,10 +161,14 @@ class Resident:
                 f"{total / 1e6:.0f} MB total vs {self.l2_bytes / 1e6:.0f} MB L2")
 
 
-def time_launches(launchers, steps, warmup, stream, sync_ranks=None):
-    """Launch launchers[i % n] for warmup + steps steps on `stream`; the timed
-    steps are bracketed by CUDA events per launch and around the region.
-    Returns (region_ms, per_launch_ms list)."""
+def time_launches(launchers, steps, warmup, stream, sync_ranks=None, per_launch=False):
+    """Launch launchers[i % n] for warmup + steps steps on `stream` and time
+    the steps with CUDA events around the region; the average launch is the
+    region divided by the steps (the launches run back to back, each may
+    overlap its start with the previous one's drain).  With per_launch=True
+    every launch is also bracketed by its own events (a diagnostic: events
+    between kernels add the launch gap to every step).
+    Returns (region_ms, per_launch_ms list or None)."""
     import torch
     n = len(launchers)
     h = stream.cuda_stream
@@ -173,8 +177,8 @@ def time_launches(launchers, steps, warmup, stream, sync_ranks=None):
         for i in range(warmup):
             launchers[i % n](h)
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_launch else None
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_launch else None
     begin = torch.cuda.Event(enable_timing=True)
     finish = torch.cuda.Event(enable_timing=True)
     if sync_ranks:
@@ -183,16 +187,20 @@ def time_launches(launchers, steps, warmup, stream, sync_ranks=None):
     torch.cuda.nvtx.range_push("tw_timed")  # lets ncu --nvtx-include select this region
     with torch.cuda.stream(stream):
         begin.record(stream)
-        for i in range(steps):
-            starts[i].record(stream)
-            launchers[(warmup + i) % n](h)
-            ends[i].record(stream)
+        if per_launch:
+            for i in range(steps):
+                starts[i].record(stream)
+                launchers[(warmup + i) % n](h)
+                ends[i].record(stream)
+        else:
+            for i in range(steps):
+                launchers[(warmup + i) % n](h)
         finish.record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     if sync_ranks:
         sync_ranks()
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)] if per_launch else None
     return begin.elapsed_time(finish), per
 
 
@@ -235,14 +243,20 @@ def check_status():
         raise RuntimeError(f"device status {status}: a kernel gave up on a bounded wait")
 
 
-def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None):
-    """Time the fused kernel on the resident batches of `res`."""
+def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None,
+               per_launch=False):
+    """Time the fused kernel on the resident batches of `res`: mean_launch_ms
+    is the region over the steps; with per_launch, the per-launch event
+    statistics are added under "events"."""
     import torch
     stream = torch.cuda.Stream()
     region_ms, per = time_launches(res.launchers(max_sms, path), steps, warmup, stream,
-                                   sync_ranks)
+                                   sync_ranks, per_launch)
     check_status()
-    return dict(region_ms=region_ms, **summarize(per))
+    out = {"region_ms": region_ms, "mean_launch_ms": region_ms / steps}
+    if per is not None:
+        out["events"] = summarize(per)
+    return out
 
 
 # ------------------------------------------------------------------ e2e ---
@@ -388,7 +402,7 @@ def sweep(args, sync_ranks):
             for b in (2, 4, 8, 16, 148, 10 ** 6)}
         del res
     dec = {}
-    for T in inputs.DECODE_TOKENS:
+    for T in sorted(set(inputs.DECODE_TOKENS) | {16, 32}):
         res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
         dec[str(T)] = {path: entry(res.wl, graph_latency(res.launchers(path=path)))
                        for path in ("warp", "cluster", "rows", "auto")}
@@ -603,6 +617,7 @@ def tw_main(args):
     algo_bytes = wl.bytes_per_token() * wl.T
     achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
 
+    diag = device_leg(res, min(args.steps, 2000), 20, per_launch=True)["events"]
     sm8 = device_leg(res, max(50, min(args.steps, 2000)), 20, max_sms=8)
     sm8_gbs = algo_bytes / (sm8["mean_launch_ms"] * 1e-3) / 1e9
     del res
@@ -645,7 +660,13 @@ def tw_main(args):
                      "frac_of_8tbs": round(achieved / 8000.0, 4),
                      "algorithmic_bytes_per_launch": algo_bytes,
                      "mean_launch_us": round(launch_ms * 1e3, 2),
-                     "median_launch_us": round(dev["median_launch_ms"] * 1e3, 2)},
+                     "launch_timing": "timed-region events over back-to-back launches "
+                                      "divided by the steps",
+                     "events_per_launch_us": {
+                         "mean": round(diag["mean_launch_ms"] * 1e3, 2),
+                         "median": round(diag["median_launch_ms"] * 1e3, 2),
+                         "note": "diagnostic pass with an event pair around every launch "
+                                 "(adds the launch gap, disables launch overlap)"}},
         "sm_budget_8": {"tokens_per_s": wl.T / (sm8["mean_launch_ms"] * 1e-3),
                         "gbs": round(sm8_gbs, 1), "frac": round(sm8_gbs / peak, 4)},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks,

@@ -94,7 +94,8 @@ typedef enum {
 
 /* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
 typedef enum {
-    TW_PATH_AUTO = 0,  /* rows kernel, or warp kernel for decode-size ranges */
+    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 16 tokens,
+                          rows kernel otherwise */
     TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
                           staged into shared memory by bulk async copies */
     TW_PATH_WARP = 2,  /* one warp per token, no shared memory */

@@ -36,10 +36,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 // Under TW_PATH_AUTO, token ranges of at most kClusterPathMaxTokens tokens go
-// to the cluster kernel (one cluster per token), ranges of at most
-// kWarpPathMaxTokens to the warp kernel, larger ones to the rows kernel.
+// to the cluster kernel (one cluster per token), larger ones to the rows
+// kernel.  The warp kernel is never faster on this GPU (one warp cannot pull a
+// 100+ KB token quickly) and runs only when asked for.
 constexpr int64_t kClusterPathMaxTokens = 16;
-constexpr int64_t kWarpPathMaxTokens = 32;
 
 struct DeviceState {
     bool ready = false;
@@ -250,9 +250,7 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
         path = TW_PATH_ROWS;
     }
     if (path == TW_PATH_AUTO)
-        path = (tokens <= kClusterPathMaxTokens && cluster_ok) ? TW_PATH_CLUSTER
-               : tokens <= kWarpPathMaxTokens                  ? TW_PATH_WARP
-                                                               : TW_PATH_ROWS;
+        path = (tokens <= kClusterPathMaxTokens && cluster_ok) ? TW_PATH_CLUSTER : TW_PATH_ROWS;
 
     int err;
     if (path == TW_PATH_ROWS) {

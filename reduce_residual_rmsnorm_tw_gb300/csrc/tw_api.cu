@@ -39,7 +39,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 // to the cluster kernel (one cluster per token), larger ones to the rows
 // kernel.  The warp kernel is never faster on this GPU (one warp cannot pull a
 // 100+ KB token quickly) and runs only when asked for.
-constexpr int64_t kClusterPathMaxTokens = 16;
+constexpr int64_t kClusterPathMaxTokens = 8;
 
 struct DeviceState {
     bool ready = false;
@@ -255,11 +255,10 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
     int err;
     if (path == TW_PATH_ROWS) {
         // Whole input rows per stage: as many as fit kStageTargetBytes (at
-        // least one), and as many stages as fit the shared memory.
-        const int staged = rows_staged_rows(a.n_parts, a.colsplit);
+        // least one; a stage may span tokens), and as many stages as fit the
+        // shared memory.
         int64_t per_stage = kStageTargetBytes / p.row_bytes;
         if (per_stage < 1) per_stage = 1;
-        if (per_stage > staged) per_stage = staged;
         p.rows_per_stage = static_cast<int>(per_stage);
         const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);
         int stages = static_cast<int>(

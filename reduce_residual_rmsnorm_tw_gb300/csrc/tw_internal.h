@@ -12,9 +12,9 @@ namespace tw {
 // row is at most kRowsThreads * kRowsMaxVecs * 16 = 32 KB).
 constexpr int kRowsThreads = 512;
 constexpr int kRowsMaxVecs = 4;
-// Target bytes of one ring stage: whole input rows of one token are staged,
-// as many as fit this size (at least one).
-constexpr int kStageTargetBytes = 48 * 1024;
+// Target bytes of one ring stage: as many whole input rows of the CTA's row
+// stream as fit this size (at least one).
+constexpr int kStageTargetBytes = 64 * 1024;
 // Ring depth bounds of the rows kernel.
 constexpr int kMaxStages = 16;
 constexpr int kMinStages = 2;
@@ -68,10 +68,7 @@ int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pd
                 void* stream);
 int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream);
-// Input rows per token the rows kernel stages (partials + residual, or the
-// assembled column-split row + residual), and its shared memory for a stage
-// size and ring depth.
-int rows_staged_rows(int n_parts, int colsplit);
+// Shared memory of the rows kernel for a stage size and ring depth.
 size_t rows_smem_bytes(size_t stage_bytes, int stages);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).

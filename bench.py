@@ -44,6 +44,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["tw", "reference"], default="tw")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (e.g. decode sizes)")
+    ap.add_argument("--path", default="auto", choices=["auto", "rows", "warp", "cluster"],
+                    help="kernel of the timed leg")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--overlap", action="store_true",
                     help="add the GEMM / fused-kernel overlap measurement")
@@ -347,6 +351,8 @@ def reference_main(args):
     import oracle
     from reduce_residual_rmsnorm_tw_gb300.inputs import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        wl = wl.with_tokens(args.tokens)
     calib_tok = min(wl.T, 16)
     parts, res, w = oracle_sample(wl, calib_tok)
     oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)
@@ -604,11 +610,13 @@ def tw_main(args):
     from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
     tw.load()
     wl = inputs.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        wl = wl.with_tokens(args.tokens)
     res = Resident(wl)
     l2_note = res.l2_note()
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
-    dev = device_leg(res, args.steps, args.warmup, sync_ranks=sync_ranks)
+    dev = device_leg(res, args.steps, args.warmup, path=args.path, sync_ranks=sync_ranks)
     clocks = sampler.stop() if sampler else None
 
     region_ms, launch_ms = max_over_ranks([dev["region_ms"], dev["mean_launch_ms"]], world)
@@ -617,8 +625,8 @@ def tw_main(args):
     algo_bytes = wl.bytes_per_token() * wl.T
     achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
 
-    diag = device_leg(res, min(args.steps, 2000), 20, per_launch=True)["events"]
-    sm8 = device_leg(res, max(50, min(args.steps, 2000)), 20, max_sms=8)
+    diag = device_leg(res, min(args.steps, 2000), 20, path=args.path, per_launch=True)["events"]
+    sm8 = device_leg(res, max(50, min(args.steps, 2000)), 20, max_sms=8, path=args.path)
     sm8_gbs = algo_bytes / (sm8["mean_launch_ms"] * 1e-3) / 1e9
     del res
     torch.cuda.empty_cache()
@@ -650,7 +658,7 @@ def tw_main(args):
         "ms_per_step": region_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "n_parts": wl.n_parts, "T": wl.T, "H": wl.H,
-                   "n_out": wl.n_out, "eps": wl.eps, "l2": l2_note,
+                   "n_out": wl.n_out, "eps": wl.eps, "l2": l2_note, "path": args.path,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "sm_count": torch.cuda.get_device_properties(local_rank).multi_processor_count},
         "hbm_gbs": round(achieved, 1),

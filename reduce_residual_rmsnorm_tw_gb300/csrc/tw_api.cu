@@ -254,10 +254,16 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 
     int err;
     if (path == TW_PATH_ROWS) {
-        // Whole input rows per stage: as many as fit kStageTargetBytes (at
-        // least one; a stage may span tokens), and as many stages as fit the
-        // shared memory.
-        int64_t per_stage = kStageTargetBytes / p.row_bytes;
+        // Whole input rows per stage, aligned to the token where possible: a
+        // whole token if its R rows fit kStageTargetBytes, else the token's
+        // rows split evenly over the fewest stages that fit (a stage crosses
+        // into the next token only when that split is uneven).  As many
+        // stages as fit the shared memory.
+        const int64_t rows = a.colsplit ? 2 : a.n_parts + 1;
+        const int64_t parts = (rows * p.row_bytes + kStageTargetBytes - 1) / kStageTargetBytes;
+        int64_t per_stage = (rows + parts - 1) / parts;
+        if (per_stage * p.row_bytes > kStageTargetBytes)
+            per_stage = kStageTargetBytes / p.row_bytes;
         if (per_stage < 1) per_stage = 1;
         p.rows_per_stage = static_cast<int>(per_stage);
         const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);

@@ -227,6 +227,12 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
                 if (valid[j])
                     add_vec(x[j], *reinterpret_cast<const uint4*>(row + j * kRowsThreads * 16),
                             static_cast<T*>(nullptr));
+            if (k == n_rows - 1) {
+                // The stage's rows are all in registers: hand it back to the
+                // producer before any epilogue below.
+                __syncwarp();
+                if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+            }
             if (++g_cur < R) continue;
             // The token's residual row is in: store residual_out, reduce the
             // sum of squares over the token, store every destination.
@@ -268,8 +274,6 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
             g_cur = 0;
             ++tok;
         }
-        __syncwarp();
-        if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
     }
 }
 

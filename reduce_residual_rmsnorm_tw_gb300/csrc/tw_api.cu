@@ -254,10 +254,9 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 
     int err;
     if (path == TW_PATH_ROWS) {
-        // Whole input rows per stage, aligned to the token where possible: a
-        // whole token if its R rows fit kStageTargetBytes, else the token's
-        // rows split evenly over the fewest stages that fit (a stage crosses
-        // into the next token only when that split is uneven).  As many
+        // Whole input rows of one token per stage: the whole token if its R
+        // rows fit kStageTargetBytes, else the token's rows split evenly over
+        // the fewest stages that fit (never more than R rows).  As many
         // stages as fit the shared memory.
         const int64_t rows = a.colsplit ? 2 : a.n_parts + 1;
         const int64_t parts = (rows * p.row_bytes + kStageTargetBytes - 1) / kStageTargetBytes;

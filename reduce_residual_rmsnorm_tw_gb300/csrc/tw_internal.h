@@ -12,8 +12,8 @@ namespace tw {
 // row is at most kRowsThreads * kRowsMaxVecs * 16 = 32 KB).
 constexpr int kRowsThreads = 512;
 constexpr int kRowsMaxVecs = 4;
-// Target bytes of one ring stage: as many whole input rows of the CTA's row
-// stream as fit this size (at least one).
+// Target bytes of one ring stage of the rows kernel (whole input rows of one
+// token, at least one row).
 constexpr int kStageTargetBytes = 64 * 1024;
 // Ring depth bounds of the rows kernel.
 constexpr int kMaxStages = 16;

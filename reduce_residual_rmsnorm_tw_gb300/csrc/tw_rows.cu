@@ -8,24 +8,23 @@
 //   out[k][t,h] = x * inv * weight[h]                 for every destination k
 //
 // Layout of the work: a token has R = N + 1 input rows (the N partials, then
-// the residual), each H * b contiguous bytes.  A CTA's tokens t0 + b,
-// t0 + b + grid, ... form one stream of rows, token after token.  One elected
-// thread of the producer warp moves that stream, whole rows at a time, into a
-// ring of shared-memory stages with 1-D bulk async copies (cp.async.bulk, one
-// copy per row, no tensor map, no multicast); every stage holds the next
-// `rows_per_stage` rows of the stream -- a stage may end one token and start
-// the next -- and is tracked by a "full" mbarrier (transaction bytes) and an
-// "empty" mbarrier (one arrival per consumer warp).  Large whole-row copies
-// from several buffers in flight are what let one SM stream well above its
-// share of HBM bandwidth, and uniform stages keep that true for any N and H.
-// The 512 consumer threads own the 16-byte vectors tid, tid + 512, ... of a
-// row: they add the staged rows into fp32 registers in row order (ranks
-// first, residual last); when a token's residual row is in, they store
-// residual_out, reduce the sum of squares (warp shuffle, then the 16 warp
-// totals through shared memory behind one named barrier) and store the
-// weighted result to every gather destination, then go on with the next
-// token's rows.  The N-way sum happens while the data streams through shared
-// memory, the counterpart of the pages' sum-at-load.
+// the residual), each H * b contiguous bytes.  One elected thread of the
+// producer warp streams them, whole rows at a time, into a ring of
+// shared-memory stages with 1-D bulk async copies (cp.async.bulk, one copy per
+// row, no tensor map, no multicast); a stage holds `rows_per_stage` rows of
+// one token (the host picks a whole token when it fits, else an even split of
+// its rows; a stage never crosses into the next token) and is tracked by a
+// "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
+// consumer warp).  Whole-row copies keep
+// several large copies from different buffers in flight, which is what lets
+// one SM stream well above its share of HBM bandwidth.  The 512 consumer
+// threads own the 16-byte vectors tid, tid + 512, ... of the row: they add the
+// staged rows into fp32 registers in row order (ranks first, residual last),
+// store residual_out once the residual row is in, and after the token's last
+// stage the sum of squares goes through a warp shuffle and the 16 warp totals
+// through shared memory behind one named barrier; then the weighted result is
+// stored to every gather destination.  The N-way sum happens while the data
+// streams through shared memory, the counterpart of the pages' sum-at-load.
 //
 // Readiness flags (the FLUX notes' WaitSignal / SetSignal): with a `ready`
 // array, the producer reads no row of token t before ready[t / block_tokens]
@@ -81,6 +80,7 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     const int n_sum = p.colsplit ? 1 : p.n_parts;  // staged rows summed before the residual
     const int R = n_sum + 1;                        // staged rows per token
     const int G = p.rows_per_stage;
+    const int stages_per_token = (R + G - 1) / G;
     const int64_t rb = p.row_bytes;
     const uint32_t stage_bytes = static_cast<uint32_t>(G * rb);
     const uint32_t full0 = smem_addr(smem + kFullOff);
@@ -105,11 +105,8 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     grid_launch_dependents();
     if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
 
-    // This CTA's tokens and its row stream.
     const int64_t first = p.t0 + blockIdx.x;
     const int64_t stride = gridDim.x;
-    const int64_t my_tokens = first < p.t1 ? (p.t1 - first + stride - 1) / stride : 0;
-    const int64_t total_rows = my_tokens * R;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer ---
@@ -117,60 +114,51 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
         const uint64_t pol = policy_evict_first();
         RingPos pos;
         uint32_t issued = 0;
-        int64_t tok = 0;            // token (index within this CTA) of the next row
-        int g_next = 0;             // row within that token
-        int64_t checked = -1;       // last token whose readiness flag was seen
-        int64_t ready_block = -1;   // last flag block seen ready
-        for (int64_t q0 = 0; q0 < total_rows; q0 += G, ++issued, pos.advance(S)) {
-            const int n_rows = total_rows - q0 < G ? static_cast<int>(total_rows - q0) : G;
+        bool stop = false;
+        int64_t ready_block = -1;  // last flag block seen ready
+        for (int64_t t = first; t < p.t1 && !stop; t += stride) {
+            const int64_t row_off = t * rb;
             if (p.ready) {
-                // Every token that starts in this stage must be ready first.
-                const int64_t last_tok = (q0 + n_rows - 1) / R;
-                bool ok = true;
-                for (int64_t i = checked + 1; i <= last_tok && ok; ++i) {
-                    const int64_t b = (first + i * stride) / p.block_tokens;
-                    if (b != ready_block) {
-                        ok = flag_wait(p.ready + b, p.epoch, abort_flag);
-                        ready_block = b;
+                const int64_t b = t / p.block_tokens;
+                if (b != ready_block) {
+                    if (!flag_wait(p.ready + b, p.epoch, abort_flag)) {
+                        give_up(p, abort_flag);
+                        atomicOr(p.status, 4u);
+                        break;
                     }
-                    checked = i;
+                    ready_block = b;
                 }
-                if (!ok) {
+            }
+            for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
+                const uint32_t s = pos.stage;
+                if (*abort_flag ||
+                    (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag))) {
                     give_up(p, abort_flag);
-                    atomicOr(p.status, 4u);
+                    stop = true;
                     break;
                 }
-            }
-            const uint32_t s = pos.stage;
-            if (*abort_flag ||
-                (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag))) {
-                give_up(p, abort_flag);
-                break;
-            }
-            const uint32_t bar = full0 + 8 * s;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_rows * rb));
-            uint32_t dst = ring_addr + s * stage_bytes;
-            for (int k = 0; k < n_rows; ++k, dst += static_cast<uint32_t>(rb)) {
-                const int64_t row_off = (first + tok * stride) * rb;
-                if (g_next == n_sum) {
-                    bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off,
-                             static_cast<uint32_t>(rb), bar, pol);
-                } else if (p.colsplit) {
-                    // One staged row from every rank's own column slice.
-                    for (int r = 0; r < p.n_parts; ++r) {
-                        const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
-                        if (lo < hi)
-                            bulk_g2s(dst + static_cast<uint32_t>(lo),
-                                     static_cast<const char*>(p.partials[r]) + row_off + lo,
-                                     static_cast<uint32_t>(hi - lo), bar, pol);
+                const int g0 = k * G;
+                const int g1 = g0 + G < R ? g0 + G : R;
+                const uint32_t bar = full0 + 8 * s;
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>((g1 - g0) * rb));
+                uint32_t dst = ring_addr + s * stage_bytes;
+                for (int g = g0; g < g1; ++g, dst += static_cast<uint32_t>(rb)) {
+                    if (g == n_sum) {
+                        bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off,
+                                 static_cast<uint32_t>(rb), bar, pol);
+                    } else if (p.colsplit) {
+                        // One staged row from every rank's own column slice.
+                        for (int r = 0; r < p.n_parts; ++r) {
+                            const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
+                            if (lo < hi)
+                                bulk_g2s(dst + static_cast<uint32_t>(lo),
+                                         static_cast<const char*>(p.partials[r]) + row_off + lo,
+                                         static_cast<uint32_t>(hi - lo), bar, pol);
+                        }
+                    } else {
+                        bulk_g2s(dst, static_cast<const char*>(p.partials[g]) + row_off,
+                                 static_cast<uint32_t>(rb), bar, pol);
                     }
-                } else {
-                    bulk_g2s(dst, static_cast<const char*>(p.partials[g_next]) + row_off,
-                             static_cast<uint32_t>(rb), bar, pol);
-                }
-                if (++g_next == R) {
-                    g_next = 0;
-                    ++tok;
                 }
             }
         }
@@ -193,86 +181,77 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     // ---------------------------------------------------------- consumers ---
     const int64_t nvec = rb / 16;
     uint4 wv[NV];
-    bool valid[NV];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
         const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
-        valid[j] = v < nvec;
-        wv[j] = valid[j] ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
+        wv[j] = v < nvec ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
                          : make_uint4(0, 0, 0, 0);
     }
 
     RingPos pos;
     int red_buf = 0;
     bool alive = true;
-    int64_t tok = 0;  // token (index within this CTA) being summed
-    int g_cur = 0;    // its rows summed so far
-    float x[NV][E];
+    for (int64_t t = first; t < p.t1; t += stride) {
+        float x[NV][E];
 #pragma unroll
-    for (int j = 0; j < NV; ++j)
+        for (int j = 0; j < NV; ++j)
 #pragma unroll
-        for (int e = 0; e < E; ++e) x[j][e] = 0.f;
-    for (int64_t q0 = 0; q0 < total_rows; q0 += G, pos.advance(S)) {
-        const int n_rows = total_rows - q0 < G ? static_cast<int>(total_rows - q0) : G;
-        const uint32_t s = pos.stage;
-        if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
-            give_up(p, abort_flag);
-            alive = false;
+            for (int e = 0; e < E; ++e) x[j][e] = 0.f;
+        for (int k = 0; k < stages_per_token; ++k, pos.advance(S)) {
+            const uint32_t s = pos.stage;
+            if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
+                give_up(p, abort_flag);
+                alive = false;
+            }
+            const int g0 = k * G;
+            const int g1 = g0 + G < R ? g0 + G : R;
+            const unsigned char* stage = ring + s * stage_bytes + tid * 16;
+            for (int g = g0; g < g1; ++g) {
+                const unsigned char* row = stage + (g - g0) * rb;
+#pragma unroll
+                for (int j = 0; j < NV; ++j)
+                    if (static_cast<int64_t>(j) * kRowsThreads + tid < nvec)
+                        add_vec(x[j],
+                                *reinterpret_cast<const uint4*>(row + j * kRowsThreads * 16),
+                                static_cast<T*>(nullptr));
+            }
+            __syncwarp();
+            if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        const unsigned char* stage = ring + s * stage_bytes + tid * 16;
-        for (int k = 0; k < n_rows; ++k) {
-            const unsigned char* row = stage + k * rb;
+        // The residual (the last staged row) is in: store residual_out and
+        // reduce the sum of squares over the token.
+        float ss2[2] = {0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < NV; ++j)
-                if (valid[j])
-                    add_vec(x[j], *reinterpret_cast<const uint4*>(row + j * kRowsThreads * 16),
-                            static_cast<T*>(nullptr));
-            if (k == n_rows - 1) {
-                // The stage's rows are all in registers: hand it back to the
-                // producer before any epilogue below.
-                __syncwarp();
-                if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+        for (int j = 0; j < NV; ++j) {
+            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
+            if (v < nvec) {
+                sum_squares<E>(ss2, x[j]);
+                if (alive)
+                    st_global_cs(static_cast<char*>(p.residual_out) + t * rb + v * 16,
+                                 V::from_float(x[j]));
             }
-            if (++g_cur < R) continue;
-            // The token's residual row is in: store residual_out, reduce the
-            // sum of squares over the token, store every destination.
-            const int64_t t = first + tok * stride;
-            float ss2[2] = {0.f, 0.f};
+        }
+        const float ss = warp_sum(ss2[0] + ss2[1]);
+        if (lane == 0) red[red_buf * kConsumerWarps + warp] = ss;
+        named_barrier(1, kRowsThreads);
+        float total = 0.f;
 #pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                if (valid[j]) {
-                    sum_squares<E>(ss2, x[j]);
-                    if (alive)
-                        st_global_cs(static_cast<char*>(p.residual_out) + t * rb +
-                                         (static_cast<int64_t>(j) * kRowsThreads + tid) * 16,
-                                     V::from_float(x[j]));
-                }
+        for (int w = 0; w < kConsumerWarps; ++w) total += red[red_buf * kConsumerWarps + w];
+        red_buf ^= 1;
+        const float inv = rsqrtf(total * p.inv_H + p.eps);
+
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
+            if (v < nvec && alive) {
+                float w[E], y[E];
+                V::to_float(wv[j], w);
+#pragma unroll
+                for (int e = 0; e < E; ++e) y[e] = (x[j][e] * inv) * w[e];
+                const uint4 packed = V::from_float(y);
+                for (int k = 0; k < p.n_out; ++k)
+                    st_global_cs(static_cast<char*>(p.out[k]) + t * rb + v * 16, packed);
             }
-            const float ss = warp_sum(ss2[0] + ss2[1]);
-            if (lane == 0) red[red_buf * kConsumerWarps + warp] = ss;
-            named_barrier(1, kRowsThreads);
-            float total = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) total += red[red_buf * kConsumerWarps + w];
-            red_buf ^= 1;
-            const float inv = rsqrtf(total * p.inv_H + p.eps);
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                if (valid[j] && alive) {
-                    float w[E], y[E];
-                    V::to_float(wv[j], w);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) y[e] = (x[j][e] * inv) * w[e];
-                    const uint4 packed = V::from_float(y);
-                    const int64_t off = t * rb + (static_cast<int64_t>(j) * kRowsThreads + tid) * 16;
-                    for (int o = 0; o < p.n_out; ++o)
-                        st_global_cs(static_cast<char*>(p.out[o]) + off, packed);
-                }
-#pragma unroll
-                for (int e = 0; e < E; ++e) x[j][e] = 0.f;
-            }
-            g_cur = 0;
-            ++tok;
         }
     }
 }

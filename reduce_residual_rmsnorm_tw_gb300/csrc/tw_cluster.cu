@@ -69,14 +69,26 @@ __global__ void __launch_bounds__(kClusterThreads)
     const int lane = tid & 31;
     const uint32_t crank = cluster_rank();
     const uint32_t csize = cluster_size();
-    grid_dependency_wait();
-    grid_launch_dependents();
-    if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
-
     const int64_t nvec = p.row_bytes / 16;
     const int64_t per_cta = (nvec + csize - 1) / csize;
     const int64_t v_begin = static_cast<int64_t>(crank) * per_cta;
     const int64_t v_end = v_begin + per_cta < nvec ? v_begin + per_cta : nvec;
+    // While the previous kernel of the stream drains, warm L2 with this CTA's
+    // column slice of its first token (a prefetch only fills L2, where that
+    // kernel's writes land too; the loads below come after the wait).
+    if (tid == 0 && v_begin < v_end) {
+        const int64_t t = p.t0 + cluster_index();
+        if (t < p.t1) {
+            const int64_t off = t * p.row_bytes + v_begin * 16;
+            const uint32_t bytes = static_cast<uint32_t>((v_end - v_begin) * 16);
+            for (int r = 0; r < p.n_parts; ++r)
+                bulk_prefetch_l2(static_cast<const char*>(p.partials[r]) + off, bytes);
+            bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, bytes);
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
 
     uint4 wv[VPT];
 #pragma unroll

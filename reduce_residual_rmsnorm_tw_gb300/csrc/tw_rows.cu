@@ -48,6 +48,8 @@ constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
 constexpr int kAbortOff = kRedOff + 2 * kConsumerWarps * 4;
 constexpr int kRingOff = 1024;
+// Tokens of its own a CTA prefetches into L2 before its first global read.
+constexpr int kPrefetchTokens = 3;
 static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
 
 __device__ __forceinline__ void give_up(const Params& p, volatile int* abort_flag) {
@@ -99,8 +101,37 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
         mbar_init_fence();
     }
     __syncthreads();
-    // Everything above touched only shared memory; global memory may still be
-    // in use by the previous kernel of the stream until this returns.
+    // While the previous kernel of the stream drains, warm L2 with this CTA's
+    // first token(s).  A prefetch only fills L2, which is where every write of
+    // that kernel lands too, so data read after the wait below is current even
+    // if the previous kernel writes these rows.  (Not with readiness flags:
+    // their rows may not exist yet.)
+    if (warp == kConsumerWarps && lane == 0 && !p.ready) {
+        const int64_t t_first = p.t0 + blockIdx.x;
+        for (int i = 0; i < kPrefetchTokens; ++i) {
+            const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;
+            if (t >= p.t1) break;
+            const int64_t off = t * rb;
+            for (int g = 0; g < R; ++g) {
+                if (g == n_sum) {
+                    bulk_prefetch_l2(static_cast<const char*>(p.residual) + off,
+                                     static_cast<uint32_t>(rb));
+                } else if (p.colsplit) {
+                    for (int r = 0; r < p.n_parts; ++r)
+                        if (p.col_lo[r] < p.col_lo[r + 1])
+                            bulk_prefetch_l2(
+                                static_cast<const char*>(p.partials[r]) + off + p.col_lo[r],
+                                static_cast<uint32_t>(p.col_lo[r + 1] - p.col_lo[r]));
+                } else {
+                    bulk_prefetch_l2(static_cast<const char*>(p.partials[g]) + off,
+                                     static_cast<uint32_t>(rb));
+                }
+            }
+        }
+    }
+    // Everything above touched only shared memory (and L2 through prefetches);
+    // global memory may still be in use by the previous kernel of the stream
+    // until this returns.
     grid_dependency_wait();
     grid_launch_dependents();
     if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();

@@ -238,6 +238,7 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
     // max_sms SMs hold its CTAs.
     const bool pdl = a.max_sms >= d.sm_count;
     Params p = make_params(a, d, t0, t1, smid_log);
+    p.prefetch = pdl ? 1 : 0;
     // Largest power-of-two cluster within the budget (at most 8: portable).
     int cluster = 1;
     while (cluster * 2 <= 8 && cluster * 2 <= sms) cluster *= 2;

@@ -73,10 +73,10 @@ __global__ void __launch_bounds__(kClusterThreads)
     const int64_t per_cta = (nvec + csize - 1) / csize;
     const int64_t v_begin = static_cast<int64_t>(crank) * per_cta;
     const int64_t v_end = v_begin + per_cta < nvec ? v_begin + per_cta : nvec;
-    // While the previous kernel of the stream drains, warm L2 with this CTA's
-    // column slice of its first token (a prefetch only fills L2, where that
+    // While the previous kernel of the stream drains (launches that may
+    // overlap it only), warm L2 with this CTA's column slice of its first token (a prefetch only fills L2, where that
     // kernel's writes land too; the loads below come after the wait).
-    if (tid == 0 && v_begin < v_end) {
+    if (tid == 0 && p.prefetch && v_begin < v_end) {
         const int64_t t = p.t0 + cluster_index();
         if (t < p.t1) {
             const int64_t off = t * p.row_bytes + v_begin * 16;

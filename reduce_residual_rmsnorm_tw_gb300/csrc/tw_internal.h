@@ -53,6 +53,7 @@ struct Params {
     int rows_per_stage;     // rows kernel: whole input rows per ring stage
     int stages;             // rows kernel: ring depth
     int colsplit;           // 1: column-split mode
+    int prefetch;           // 1: warm L2 before the dependency wait (overlapped launches)
     float eps;
     float inv_H;
 };

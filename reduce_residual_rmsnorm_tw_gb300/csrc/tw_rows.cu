@@ -101,12 +101,12 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
         mbar_init_fence();
     }
     __syncthreads();
-    // While the previous kernel of the stream drains, warm L2 with this CTA's
-    // first token(s).  A prefetch only fills L2, which is where every write of
+    // While the previous kernel of the stream drains (launches that may
+    // overlap it only), warm L2 with this CTA's first token(s).  A prefetch only fills L2, which is where every write of
     // that kernel lands too, so data read after the wait below is current even
     // if the previous kernel writes these rows.  (Not with readiness flags:
     // their rows may not exist yet.)
-    if (warp == kConsumerWarps && lane == 0 && !p.ready) {
+    if (warp == kConsumerWarps && lane == 0 && p.prefetch && !p.ready) {
         const int64_t t_first = p.t0 + blockIdx.x;
         for (int i = 0; i < kPrefetchTokens; ++i) {
             const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;

@@ -48,8 +48,14 @@ constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
 constexpr int kAbortOff = kRedOff + 2 * kConsumerWarps * 4;
 constexpr int kRingOff = 1024;
-// Tokens of its own a CTA prefetches into L2 before its first global read.
-constexpr int kPrefetchTokens = 3;
+// Tokens of its own a CTA prefetches into L2 before its first global read:
+// five when a token's input rows are at least 64 KB, three for smaller
+// tokens (both measured best), and never more than kPrefetchMaxBytes, so the
+// prefetch of a whole grid stays well inside L2.
+constexpr int kPrefetchTokensLarge = 5;
+constexpr int kPrefetchTokensSmall = 3;
+constexpr int64_t kPrefetchLargeToken = 64 * 1024;
+constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
 static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
 
 __device__ __forceinline__ void give_up(const Params& p, volatile int* abort_flag) {
@@ -102,13 +108,17 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     }
     __syncthreads();
     // While the previous kernel of the stream drains (launches that may
-    // overlap it only), warm L2 with this CTA's first token(s).  A prefetch only fills L2, which is where every write of
+    // overlap it only), warm L2 with this CTA's first tokens.  A prefetch only fills L2, which is where every write of
     // that kernel lands too, so data read after the wait below is current even
     // if the previous kernel writes these rows.  (Not with readiness flags:
     // their rows may not exist yet.)
     if (warp == kConsumerWarps && lane == 0 && p.prefetch && !p.ready) {
         const int64_t t_first = p.t0 + blockIdx.x;
-        for (int i = 0; i < kPrefetchTokens; ++i) {
+        const int64_t token_bytes = static_cast<int64_t>(R) * rb;
+        int64_t n_pre = token_bytes >= kPrefetchLargeToken ? kPrefetchTokensLarge
+                                                           : kPrefetchTokensSmall;
+        if (n_pre * token_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / token_bytes;
+        for (int64_t i = 0; i < n_pre; ++i) {
             const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;
             if (t >= p.t1) break;
             const int64_t off = t * rb;

@@ -48,13 +48,10 @@ constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
 constexpr int kAbortOff = kRedOff + 2 * kConsumerWarps * 4;
 constexpr int kRingOff = 1024;
-// Tokens of its own a CTA prefetches into L2 before its first global read:
-// five when a token's input rows are at least 64 KB, three for smaller
-// tokens (both measured best), and never more than kPrefetchMaxBytes, so the
-// prefetch of a whole grid stays well inside L2.
-constexpr int kPrefetchTokensLarge = 5;
-constexpr int kPrefetchTokensSmall = 3;
-constexpr int64_t kPrefetchLargeToken = 64 * 1024;
+// Tokens of its own a CTA prefetches into L2 before its first global read
+// (three measured best), never more than kPrefetchMaxBytes, so the prefetch
+// of a whole grid stays well inside L2.
+constexpr int kPrefetchTokens = 3;
 constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
 static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
 
@@ -115,8 +112,7 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     if (warp == kConsumerWarps && lane == 0 && p.prefetch && !p.ready) {
         const int64_t t_first = p.t0 + blockIdx.x;
         const int64_t token_bytes = static_cast<int64_t>(R) * rb;
-        int64_t n_pre = token_bytes >= kPrefetchLargeToken ? kPrefetchTokensLarge
-                                                           : kPrefetchTokensSmall;
+        int64_t n_pre = kPrefetchTokens;
         if (n_pre * token_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / token_bytes;
         for (int64_t i = 0; i < n_pre; ++i) {
             const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;

@@ -596,7 +596,9 @@ def tw_main(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local_rank)
+    # One GPU per rank; with fewer GPUs than ranks, replicas share them.
+    device = local_rank % max(1, torch.cuda.device_count())
+    torch.cuda.set_device(device)
     sync_ranks = None
     if world > 1:
         import torch.distributed as dist
@@ -615,7 +617,7 @@ def tw_main(args):
     res = Resident(wl)
     l2_note = res.l2_note()
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(device) if rank == 0 else None
     dev = device_leg(res, args.steps, args.warmup, path=args.path, sync_ranks=sync_ranks)
     clocks = sampler.stop() if sampler else None
 
@@ -660,7 +662,7 @@ def tw_main(args):
         "config": {"workload": wl.name, "n_parts": wl.n_parts, "T": wl.T, "H": wl.H,
                    "n_out": wl.n_out, "eps": wl.eps, "l2": l2_note, "path": args.path,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "sm_count": torch.cuda.get_device_properties(local_rank).multi_processor_count},
+                   "sm_count": torch.cuda.get_device_properties(device).multi_processor_count},
         "hbm_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

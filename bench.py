@@ -323,10 +323,19 @@ def oracle_sample(wl, n_tokens):
             inputs.to_f64(d["weight"]))
 
 
+def host_cores():
+    """Cores this process may run on (torchrun's OMP_NUM_THREADS=1 aside)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(wl, seconds):
     """The oracle (reordered order, fp64, as it stands) on this host's cores,
     repeated on a bounded sample of the workload for about `seconds`."""
     import oracle
+    oracle.set_threads(host_cores())
     n_tok = min(wl.T, 64)
     parts, res, w = oracle_sample(wl, n_tok)
     oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)  # build + warm
@@ -350,6 +359,7 @@ def reference_main(args):
         return 0
     import oracle
     from reduce_residual_rmsnorm_tw_gb300.inputs import WORKLOADS
+    oracle.set_threads(host_cores())
     wl = WORKLOADS[args.workload]
     if args.tokens is not None:
         wl = wl.with_tokens(args.tokens)

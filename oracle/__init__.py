@@ -39,6 +39,8 @@ class Oracle:
         lib.tw_oracle_token_slice.restype = ctypes.c_int
         lib.tw_oracle_threads.argtypes = []
         lib.tw_oracle_threads.restype = ctypes.c_int
+        lib.tw_oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.tw_oracle_set_threads.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -95,6 +97,10 @@ class Oracle:
         """Threads the oracle's token loops run on."""
         return self.lib.tw_oracle_threads()
 
+    def set_threads(self, n):
+        """Run later calls from this thread on `n` threads."""
+        self.lib.tw_oracle_set_threads(int(n))
+
 
 def _f64(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
@@ -125,3 +131,7 @@ def token_slice(n_tokens, n_ranks, r):
 
 def threads():
     return default().threads()
+
+
+def set_threads(n):
+    return default().set_threads(n)

@@ -193,3 +193,13 @@ int tw_oracle_threads(void)
     return 1;
 #endif
 }
+
+void tw_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -273,7 +273,16 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
         if (stages < kMinStages)
             return fail(TW_ERR_UNSUPPORTED, "shared memory too small for rows of %lld bytes",
                         (long long)p.row_bytes);
+        // Producer warps: the largest power of two up to kRowsMaxProducers
+        // that the ring holds; the ring is cut to a multiple of it, so each
+        // producer owns the same stages for the whole launch.
+        static_assert((kRowsMaxProducers & (kRowsMaxProducers - 1)) == 0,
+                      "producer count must be a power of two");
+        int producers = kRowsMaxProducers;
+        while (producers > 1 && producers > stages) producers /= 2;
+        stages -= stages % producers;
         p.stages = stages;
+        p.producers = producers;
         size_t smem = rows_smem_bytes(stage, stages);
         if (smem < static_cast<size_t>(kExclusiveSmemBytes)) smem = kExclusiveSmemBytes;
         const int grid = static_cast<int>(tokens < sms ? tokens : sms);

@@ -12,6 +12,11 @@ namespace tw {
 // row is at most kRowsThreads * kRowsMaxVecs * 16 = 32 KB).
 constexpr int kRowsThreads = 512;
 constexpr int kRowsMaxVecs = 4;
+// Producer warps of the rows kernel (one elected lane each issues the bulk
+// copies of the ring stages it owns).  One SM's copy rate grows with the
+// number of threads issuing copies, so a CTA that streams alone on its SM
+// issues from several.
+constexpr int kRowsMaxProducers = 2;
 // Target bytes of one ring stage of the rows kernel (whole input rows of one
 // token, at least one row).
 constexpr int kStageTargetBytes = 64 * 1024;
@@ -51,7 +56,8 @@ struct Params {
     unsigned int epoch;
     int n_parts, n_out;
     int rows_per_stage;     // rows kernel: whole input rows per ring stage
-    int stages;             // rows kernel: ring depth
+    int stages;             // rows kernel: ring depth (a multiple of producers)
+    int producers;          // rows kernel: producer warps issuing copies (1..kRowsMaxProducers)
     int colsplit;           // 1: column-split mode
     int prefetch;           // 1: warm L2 before the dependency wait (overlapped launches)
     float eps;

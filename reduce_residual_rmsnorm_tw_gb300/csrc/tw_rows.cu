@@ -8,16 +8,19 @@
 //   out[k][t,h] = x * inv * weight[h]                 for every destination k
 //
 // Layout of the work: a token has R = N + 1 input rows (the N partials, then
-// the residual), each H * b contiguous bytes.  One elected thread of the
-// producer warp streams them, whole rows at a time, into a ring of
-// shared-memory stages with 1-D bulk async copies (cp.async.bulk, one copy per
-// row, no tensor map, no multicast); a stage holds `rows_per_stage` rows of
-// one token (the host picks a whole token when it fits, else an even split of
-// its rows; a stage never crosses into the next token) and is tracked by a
-// "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
-// consumer warp).  Whole-row copies keep
-// several large copies from different buffers in flight, which is what lets
-// one SM stream well above its share of HBM bandwidth.  The 512 consumer
+// the residual), each H * b contiguous bytes.  Producer warps stream them,
+// whole rows at a time, into a ring of shared-memory stages with 1-D bulk
+// async copies (cp.async.bulk, one copy per row, no tensor map, no
+// multicast); a stage holds `rows_per_stage` rows of one token (the host
+// picks a whole token when it fits, else an even split of its rows; a stage
+// never crosses into the next token) and is tracked by a "full" mbarrier
+// (transaction bytes) and an "empty" mbarrier (one arrival per consumer
+// warp).  The ring's stages are dealt round robin to `producers` warps (one
+// elected lane each): the copy rate of one SM grows with the number of
+// threads issuing copies (one issuing thread streamed ~36 GB/s of 16 KB
+// copies whatever the ring depth, two ~69 GB/s), which is what bounds a CTA
+// streaming alone on its SM under a small SM budget.  Whole-row copies keep
+// several large copies from different buffers in flight.  The 512 consumer
 // threads own the 16-byte vectors tid, tid + 512, ... of the row: they add the
 // staged rows into fp32 registers in row order (ranks first, residual last),
 // store residual_out once the residual row is in, and after the token's last
@@ -55,6 +58,26 @@ constexpr int kPrefetchTokens = 3;
 constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
 static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
 
+// Warm L2 with every input row of token t (bulk prefetches: nothing returns
+// to the SM and nothing waits on them).
+__device__ __forceinline__ void prefetch_token(const Params& p, int64_t t, int R, int n_sum) {
+    const int64_t rb = p.row_bytes;
+    const int64_t off = t * rb;
+    for (int g = 0; g < R; ++g) {
+        if (g == n_sum) {
+            bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, static_cast<uint32_t>(rb));
+        } else if (p.colsplit) {
+            for (int r = 0; r < p.n_parts; ++r)
+                if (p.col_lo[r] < p.col_lo[r + 1])
+                    bulk_prefetch_l2(static_cast<const char*>(p.partials[r]) + off + p.col_lo[r],
+                                     static_cast<uint32_t>(p.col_lo[r + 1] - p.col_lo[r]));
+        } else {
+            bulk_prefetch_l2(static_cast<const char*>(p.partials[g]) + off,
+                             static_cast<uint32_t>(rb));
+        }
+    }
+}
+
 __device__ __forceinline__ void give_up(const Params& p, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicOr(p.status, 1u);
@@ -71,8 +94,10 @@ struct RingPos {
     }
 };
 
+constexpr int kRowsBlock = kRowsThreads + 32 * kRowsMaxProducers;
+
 template <typename T, int NV>
-__global__ void __launch_bounds__(kRowsThreads + 32, 1)
+__global__ void __launch_bounds__(kRowsBlock, 1)
     rows_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     using V = Vec<T>;
@@ -82,7 +107,7 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const uint32_t S = static_cast<uint32_t>(p.stages);
-    const int n_sum = p.colsplit ? 1 : p.n_parts;  // staged rows summed before the residual
+    const int n_sum = p.colsplit ? 1 : p.n_parts;  // rows summed before the residual
     const int R = n_sum + 1;                        // staged rows per token
     const int G = p.rows_per_stage;
     const int stages_per_token = (R + G - 1) / G;
@@ -117,22 +142,7 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
         for (int64_t i = 0; i < n_pre; ++i) {
             const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;
             if (t >= p.t1) break;
-            const int64_t off = t * rb;
-            for (int g = 0; g < R; ++g) {
-                if (g == n_sum) {
-                    bulk_prefetch_l2(static_cast<const char*>(p.residual) + off,
-                                     static_cast<uint32_t>(rb));
-                } else if (p.colsplit) {
-                    for (int r = 0; r < p.n_parts; ++r)
-                        if (p.col_lo[r] < p.col_lo[r + 1])
-                            bulk_prefetch_l2(
-                                static_cast<const char*>(p.partials[r]) + off + p.col_lo[r],
-                                static_cast<uint32_t>(p.col_lo[r + 1] - p.col_lo[r]));
-                } else {
-                    bulk_prefetch_l2(static_cast<const char*>(p.partials[g]) + off,
-                                     static_cast<uint32_t>(rb));
-                }
-            }
+            prefetch_token(p, t, R, n_sum);
         }
     }
     // Everything above touched only shared memory (and L2 through prefetches);
@@ -145,29 +155,36 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
     const int64_t first = p.t0 + blockIdx.x;
     const int64_t stride = gridDim.x;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------ producer ---
-        if (lane != 0) return;
+    if (warp >= kConsumerWarps) {
+        // ----------------------------------------------------- producers ---
+        // Producer `pw` issues the stages s with s % producers == pw (the
+        // ring depth is a multiple of producers, so it owns the same slots
+        // throughout); every producer walks the same stage sequence.
+        const uint32_t P = static_cast<uint32_t>(p.producers);  // a power of two
+        const uint32_t pw = static_cast<uint32_t>(warp - kConsumerWarps);
+        if (lane != 0 || pw >= P) return;
         const uint64_t pol = policy_evict_first();
         RingPos pos;
-        uint32_t issued = 0;
+        uint64_t issued = 0;  // stages of the sequence passed, by any producer
         bool stop = false;
         int64_t ready_block = -1;  // last flag block seen ready
         for (int64_t t = first; t < p.t1 && !stop; t += stride) {
             const int64_t row_off = t * rb;
-            if (p.ready) {
-                const int64_t b = t / p.block_tokens;
-                if (b != ready_block) {
-                    if (!flag_wait(p.ready + b, p.epoch, abort_flag)) {
-                        give_up(p, abort_flag);
-                        atomicOr(p.status, 4u);
-                        break;
-                    }
-                    ready_block = b;
-                }
-            }
             for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
                 const uint32_t s = pos.stage;
+                if ((s & (P - 1)) != pw) continue;
+                if (p.ready) {
+                    const int64_t b = t / p.block_tokens;
+                    if (b != ready_block) {
+                        if (!flag_wait(p.ready + b, p.epoch, abort_flag)) {
+                            give_up(p, abort_flag);
+                            atomicOr(p.status, 4u);
+                            stop = true;
+                            break;
+                        }
+                        ready_block = b;
+                    }
+                }
                 if (*abort_flag ||
                     (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag))) {
                     give_up(p, abort_flag);
@@ -199,9 +216,10 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
                 }
             }
         }
-        // Drain: the copies of the last S issued stages must have landed before
-        // this CTA may exit (bounded, also on the give-up path).  Walk back
-        // from the last issued stage.
+        // Drain: this producer's copies into its slots must have landed before
+        // the CTA may exit (bounded, also on the give-up path).  Walk back
+        // over the last S stages of the sequence before the point where this
+        // producer stopped: each of its slots appears once, at its last use.
         RingPos back = pos;
         for (uint32_t k = 0; k < S && k < issued; ++k) {
             if (back.stage == 0) {
@@ -210,6 +228,7 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
             } else {
                 --back.stage;
             }
+            if ((back.stage & (P - 1)) != pw) continue;
             if (!mbar_wait(full0 + 8 * back.stage, back.phase, nullptr)) atomicOr(p.status, 2u);
         }
         return;
@@ -255,8 +274,8 @@ __global__ void __launch_bounds__(kRowsThreads + 32, 1)
             __syncwarp();
             if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        // The residual (the last staged row) is in: store residual_out and
-        // reduce the sum of squares over the token.
+        // Every row is in, the residual last: store residual_out and reduce
+        // the sum of squares over the token.
         float ss2[2] = {0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
@@ -333,7 +352,7 @@ int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pd
                 void* stream) {
     void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes));
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
-    return launch_with_pdl(fn, p, grid, kRowsThreads + 32, smem_bytes, pdl, stream);
+    return launch_with_pdl(fn, p, grid, kRowsBlock, smem_bytes, pdl, stream);
 }
 
 }  // namespace tw

@@ -59,6 +59,28 @@ def test_parity_small_sm_budget(max_sms):
     check_workload(wl(3, 30, 4096), path="cluster", max_sms=max_sms)
 
 
+# Small budgets over rows of 1 to 4 vectors per thread and 2 to 9 rows per
+# token: many tokens per CTA, the ring's stages dealt to two producer warps
+# (an odd ring depth cut to an even one), with and without an in-place
+# residual.
+BUDGET_SHAPES = [
+    wl(1, 23, 8192),                   # two rows per token
+    wl(2, 31, 4096, n_out=2),
+    wl(8, 29, 8192, eps=1e-5, std=(1 / 8) ** 0.5),   # three stages per token
+    wl(4, 17, 12288),                  # 3 vectors per thread
+    wl(3, 11, 16384),                  # 4 vectors per thread
+    wl(6, 19, 4096, "f32", n_out=3),
+    wl(3, 27, 1000),                   # ragged row, one vector per thread
+]
+
+
+@pytest.mark.parametrize("max_sms", [1, 4, 76])
+@pytest.mark.parametrize("case", BUDGET_SHAPES, ids=lambda c: c.name)
+def test_parity_budget_shapes(case, max_sms):
+    check_workload(case, path="rows", max_sms=max_sms)
+    check_workload(case, path="rows", max_sms=max_sms, t0=1, t1=case.T - 1, in_place=True)
+
+
 def test_cluster_rejects_rows_too_long_for_the_budget():
     from reduce_residual_rmsnorm_tw_gb300 import tw
     with pytest.raises(tw.TwError, match="TW_ERR_UNSUPPORTED"):

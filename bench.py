@@ -264,7 +264,7 @@ def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None,
 
 
 # ------------------------------------------------------------------ e2e ---
-def e2e_leg(wl, steps, warmup, chunks=(128, 256, 512), sync_ranks=None):
+def e2e_leg(wl, steps, warmup, chunks=(64, 128, 256, 512), sync_ranks=None):
     """The same step from pinned HOST buffers through the C ABI's host entry
     point (tw_fused_reduce_add_rmsnorm_host): every step moves that step's
     inputs host->device, runs the kernel and moves the outputs back, with the
@@ -655,8 +655,9 @@ def tw_main(args):
                "chunk_tokens": chunk,
                "ms_per_step_by_chunk": {str(k): round(v, 4) for k, v in per_chunk.items()},
                "path": "tw_fused_reduce_add_rmsnorm_host: pinned host buffers, "
-                       "chunked host->device copies / kernel / device->host copies "
-                       "overlapped on three streams"}
+                       "chunked host->device copies overlapping the kernel on the previous "
+                       "chunk, which stores its results straight into the mapped host "
+                       "outputs (device->host copies where they are not mapped)"}
     extra = sweep(args, None) if args.sweep and rank == 0 else None
     overlap = overlap_leg() if args.overlap and rank == 0 else None
     cpu = None

@@ -199,12 +199,16 @@ int tw_split_launch(const void* const* partials, int n_parts,
  * pointers with the layout and rules above; only `workspace` is device memory,
  * at least tw_host_workspace_bytes() bytes, 256-byte aligned, owned by the
  * caller.  Rows [t0, t1) are moved in chunks of chunk_tokens tokens: the
- * host->device copies of one chunk, the kernel on the previous one and the
- * device->host copies of the one before overlap on three streams the library
- * creates once per device; `stream` orders the whole call (it waits for the
- * last copy back).  The host buffers and the workspace are in use until the
- * work on `stream` completes.  Returns TW_ERR_INVALID_ARG if a tensor is not
- * page-locked host memory or the workspace is too small. */
+ * host->device copies of one chunk overlap the kernel on the previous one, on
+ * streams the library creates once per device.  When out and residual_out
+ * are mapped into the device's address space (cudaHostGetDevicePointer
+ * succeeds: all page-locked memory on a system with unified addressing) the
+ * kernel stores the results straight into them; otherwise the results are
+ * staged in the workspace and copied back on a third stream, overlapping the
+ * following chunks.  `stream` orders the whole call (it waits for the last
+ * kernel or copy back).  The host buffers and the workspace are in use until
+ * the work on `stream` completes.  Returns TW_ERR_INVALID_ARG if a tensor is
+ * not page-locked host memory or the workspace is too small. */
 int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
                                      const void* residual, const void* weight,
                                      void* const* out, int n_out,

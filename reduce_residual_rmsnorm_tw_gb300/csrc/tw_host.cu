@@ -3,11 +3,15 @@
 // The token range is cut into chunks of `chunk_tokens` tokens that flow
 // through two slots of a caller-provided device workspace on streams the
 // library owns per device: the host->device copies of chunk i + 1 (spread over
-// kH2DStreams streams, so several copy engines pull at once), the kernel on
-// chunk i and the device->host copies of chunk i - 1 overlap (the copy engines
-// run both directions of the host link at once).  Events order the slots; the
-// caller's stream waits for the last copy, so the call behaves like one
-// asynchronous operation on that stream.
+// kH2DStreams streams, so several copy engines pull at once) overlap the
+// kernel on chunk i.  When every output buffer is mapped pinned memory (the
+// device can address it, which cudaHostGetDevicePointer reports), the kernel
+// stores its results straight into the caller's host buffers over the host
+// link, so no copy back trails the last chunk; otherwise the results are
+// staged in the workspace and copied back on a third stream, overlapping the
+// next chunks.  Events order the slots; the caller's stream waits for the
+// last kernel or copy, so the call behaves like one asynchronous operation on
+// that stream.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -89,6 +93,14 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
     };
     const cudaStream_t user = static_cast<cudaStream_t>(c.stream);
 
+    // Direct stores: the device address of every output host buffer.
+    void* mapped_out[TW_MAX_OUTS] = {};
+    void* mapped_res = nullptr;
+    bool direct = cudaHostGetDevicePointer(&mapped_res, c.residual_out, 0) == cudaSuccess;
+    for (int k = 0; direct && k < c.n_out; ++k)
+        direct = cudaHostGetDevicePointer(&mapped_out[k], c.out[k], 0) == cudaSuccess;
+    if (!direct) (void)cudaGetLastError();  // not mapped: stage and copy back
+
 #define TW_TRY(call, name)                                     \
     do {                                                       \
         if ((e = (call)) != cudaSuccess) {                     \
@@ -112,10 +124,12 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
         const int64_t n = c.t1 - first < c.chunk_tokens ? c.t1 - first : c.chunk_tokens;
         const size_t bytes = static_cast<size_t>(n) * rb;
         const size_t host_off = static_cast<size_t>(first) * rb;
-        // The slot's previous chunk must be summed and copied back first.
+        // The slot's previous chunk must be summed (and copied back) first.
         if (i >= 2)
             for (int j = 0; j < kH2DStreams; ++j)
-                TW_TRY(cudaStreamWaitEvent(hp->h2d[j], hp->out_done[slot], 0), "wait slot");
+                TW_TRY(cudaStreamWaitEvent(hp->h2d[j],
+                                           direct ? hp->comp_done[slot] : hp->out_done[slot], 0),
+                       "wait slot");
         // Input rows r = 0..n_parts (the residual last) alternate over the
         // host->device streams.
         for (int r = 0; r <= c.n_parts; ++r) {
@@ -132,11 +146,15 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
         const void* d_parts[TW_MAX_PARTS];
         void* d_outs[TW_MAX_OUTS];
         for (int r = 0; r < c.n_parts; ++r) d_parts[r] = in_buf(slot, r);
-        for (int k = 0; k < c.n_out; ++k) d_outs[k] = out_buf(slot, k);
+        for (int k = 0; k < c.n_out; ++k)
+            d_outs[k] = direct ? static_cast<char*>(mapped_out[k]) + host_off : out_buf(slot, k);
+        void* d_res_out = direct ? static_cast<char*>(mapped_res) + host_off
+                                 : static_cast<void*>(out_buf(slot, c.n_out));
         const int rc = launch_chunk(d_parts, in_buf(slot, c.n_parts), d_weight, d_outs,
-                                    out_buf(slot, c.n_out), n, hp->compute);
+                                    d_res_out, n, hp->compute);
         if (rc != 0) return *what = nullptr, rc;  // a tw_status, message already set
         TW_TRY(cudaEventRecord(hp->comp_done[slot], hp->compute), "cudaEventRecord");
+        if (direct) continue;
 
         TW_TRY(cudaStreamWaitEvent(hp->d2h, hp->comp_done[slot], 0), "cudaStreamWaitEvent");
         for (int k = 0; k < c.n_out; ++k)
@@ -148,9 +166,10 @@ int host_pipeline(const HostCall& c, const LaunchChunk& launch_chunk, const char
                "cudaMemcpyAsync");
         TW_TRY(cudaEventRecord(hp->out_done[slot], hp->d2h), "cudaEventRecord");
     }
-    // The caller's stream continues after the last copy back; the copies in
-    // and the kernels precede it through the events.
-    TW_TRY(cudaEventRecord(hp->end, hp->d2h), "cudaEventRecord");
+    // The caller's stream continues after the last kernel (direct stores) or
+    // the last copy back; the copies in and the kernels precede it through
+    // the events.
+    TW_TRY(cudaEventRecord(hp->end, direct ? hp->compute : hp->d2h), "cudaEventRecord");
     TW_TRY(cudaStreamWaitEvent(user, hp->end, 0), "cudaStreamWaitEvent");
 #undef TW_TRY
     return 0;

@@ -2,6 +2,8 @@
 token range pipelined in chunks.  Checked against the oracle element by
 element, and bit for bit against the device entry point when every chunk
 runs on the same kernel."""
+from dataclasses import replace
+
 import pytest
 import torch
 
@@ -71,3 +73,58 @@ def test_host_rejects_pageable_memory():
     with pytest.raises(tw.TwError, match="page-locked"):
         tw.tw_fused_reduce_add_rmsnorm_host(d["partials"], d["residual"], d["weight"], out,
                                             torch.empty_like(out[0]), wl.eps, ws, 4)
+
+
+def test_host_in_place_residual():
+    # residual_out is the pinned residual itself: each chunk's rows are read
+    # (copied in) before the kernel on that chunk writes them back.
+    wl = CASES[0]
+    t0, t1 = 3, wl.T - 2
+    d = inputs.make_inputs(wl)
+    parts = [p.pin_memory() for p in d["partials"]]
+    res = d["residual"].clone().pin_memory()
+    w = d["weight"].pin_memory()
+    out = [torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()]
+    ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, 1, wl.H, 16, wl.torch_dtype),
+                     dtype=torch.uint8, device="cuda")
+    tw.tw_fused_reduce_add_rmsnorm_host(parts, res, w, out, res, wl.eps, ws, 16, t0, t1)
+    torch.cuda.synchronize()
+    ref_out, ref_res = oracle.reordered([inputs.to_f64(p) for p in d["partials"]],
+                                        inputs.to_f64(d["residual"]), inputs.to_f64(d["weight"]),
+                                        wl.eps, n_out=1, t0=t0, t1=t1)
+    check_close(out[0][t0:t1], ref_out[0][t0:t1], wl.dtype, "in-place out")
+    check_close(res[t0:t1], ref_res[t0:t1], wl.dtype, "in-place residual_out")
+    assert torch.equal(torch.cat([res[:t0], res[t1:]]),
+                       torch.cat([d["residual"][:t0], d["residual"][t1:]]))
+
+
+def test_host_back_to_back_steps_on_one_stream():
+    # Step 2 reads step 1's host outputs (its partial 0 is step 1's out, its
+    # residual step 1's residual_out); enqueued back to back on one stream it
+    # must equal the same two steps with the host synchronised between them.
+    wl = CASES[0].with_tokens(48)
+    d1 = inputs.make_inputs(wl)
+    d2 = inputs.make_inputs(replace(wl, seed=wl.seed + 7))
+    ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, 1, wl.H, 8, wl.torch_dtype),
+                     dtype=torch.uint8, device="cuda")
+    w1, w2 = d1["weight"].pin_memory(), d2["weight"].pin_memory()
+    p1 = [p.pin_memory() for p in d1["partials"]]
+    rest2 = [p.pin_memory() for p in d2["partials"][1:]]
+    res1 = d1["residual"].pin_memory()
+    results = []
+    for sync in (True, False):
+        out1 = [torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()]
+        res_out1 = torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()
+        out2 = [torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()]
+        res_out2 = torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()
+        torch.cuda.synchronize()
+        tw.tw_fused_reduce_add_rmsnorm_host(p1, res1, w1, out1, res_out1, wl.eps, ws, 8)
+        if sync:
+            torch.cuda.synchronize()
+        tw.tw_fused_reduce_add_rmsnorm_host([out1[0]] + rest2, res_out1, w2, out2, res_out2,
+                                            wl.eps, ws, 8)
+        torch.cuda.synchronize()
+        results.append((out2[0].clone(), res_out2.clone()))
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
+    assert bool(torch.isfinite(results[0][0].float()).all())

@@ -67,12 +67,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources that define the timed rows-kernel launch: the kernel, its
+# device helpers and parameters, and the host code that sizes and launches it.
+ROWS_KERNEL_SOURCES = ("tw_api.cu", "tw_device.cuh", "tw_internal.h", "tw_rows.cu")
+
+
 def kernel_source_hash():
-    """Hash of the kernel sources: a stored ncu traffic figure is only
+    """Hash of the rows kernel's sources: a stored ncu traffic figure is only
     reported while it still describes the kernel being timed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_tw_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ROWS_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

@@ -336,11 +336,12 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, seconds):
-    """The oracle (reordered order, fp64, as it stands) on this host's cores,
-    repeated on a bounded sample of the workload for about `seconds`."""
+def cpu_baseline(wl, seconds, threads=None):
+    """The oracle (reordered order, fp64, as it stands) on this host's cores
+    (or `threads` of them), repeated on a bounded sample of the workload for
+    about `seconds`."""
     import oracle
-    oracle.set_threads(host_cores())
+    oracle.set_threads(threads or host_cores())
     n_tok = min(wl.T, 64)
     parts, res, w = oracle_sample(wl, n_tok)
     oracle.reordered(parts, res, w, wl.eps, n_out=wl.n_out)  # build + warm
@@ -403,7 +404,9 @@ def reference_main(args):
 
 # ----------------------------------------------------------------- sweep ---
 def sweep(args, sync_ranks):
-    """SM-budget sweep, decode sweep, two-stream split, fp32 column split."""
+    """SM-budget sweep, decode sweep, fp32 column split, the two-stream split
+    and the same tokens as one launch, the unfused torch chain, and the oracle
+    on one host thread and on all cores."""
     import torch
     from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
     W = inputs.WORKLOADS
@@ -468,7 +471,53 @@ def sweep(args, sync_ranks):
         split[str(b)] = entry(wl, evs[0].elapsed_time(evs[1]) / n_rep)
     check_status()
     out["split_tp8_t16384_h8192_bf16"] = split
+    # The same 16 384 tokens as one launch at the same budgets.
+    out["single_launch:split_tp8_t16384_h8192_bf16"] = {
+        str(b): entry(wl, device_leg(res, 3 if b <= 4 else 20, 2, max_sms=b)["mean_launch_ms"])
+        for b in (2, 4, 8, 16, 148)}
+    del res
+    out["unfused_torch_chain"] = unfused_leg(W[HEADLINE], steps)
+    out["oracle_threads"] = {str(n): cpu_baseline(W[HEADLINE], 5.0, threads=n)
+                             for n in (1, host_cores())}
     return out
+
+
+def unfused_leg(wl, steps):
+    """Context comparator: the unfused chain the fused step replaces, in
+    plain torch ops (a stacked sum of the partials, the residual add, then
+    torch's RMSNorm), on the same rotating resident batches.  GB/s is counted
+    with the fused step's algorithmic bytes, so it compares times."""
+    import torch
+    import torch.nn.functional as F
+    res = Resident(wl)
+    peak, _ = measured_peaks()
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        t0, t1 = res.ranges()[i % res.n_sets]
+        x = torch.stack([p[t0:t1] for p in res.partials]).sum(0) + res.residual[t0:t1]
+        res.residual_out[t0:t1] = x
+        res.out[0][t0:t1] = F.rms_norm(x, (wl.H,), res.weight, wl.eps)
+
+    n = max(20, steps // 10)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
+    del res
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "step_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4),
+            "chain": "torch.stack(partials).sum(0) + residual; rms_norm(x, weight, eps); "
+                     "copies into residual_out and out"}
 
 
 # --------------------------------------------------------------- overlap ---
@@ -691,6 +740,7 @@ def tw_main(args):
                      "events_per_launch_us": {
                          "mean": round(diag["mean_launch_ms"] * 1e3, 2),
                          "median": round(diag["median_launch_ms"] * 1e3, 2),
+                         "min": round(diag["min_launch_ms"] * 1e3, 2),
                          "note": "diagnostic pass with an event pair around every launch "
                                  "(adds the launch gap, disables launch overlap)"}},
         "sm_budget_8": {"tokens_per_s": wl.T / (sm8["mean_launch_ms"] * 1e-3),

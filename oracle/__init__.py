@@ -98,7 +98,7 @@ class Oracle:
         return self.lib.tw_oracle_threads()
 
     def set_threads(self, n):
-        """Run later calls from this thread on `n` threads."""
+        """Run later calls on `n` threads."""
         self.lib.tw_oracle_set_threads(int(n))
 
 

@@ -41,6 +41,11 @@
 #include <omp.h>
 #endif
 
+/* Threads of the token loops: 0 = the OpenMP runtime's default.  Passed to
+   every loop explicitly, so it holds whichever OpenMP runtime the process
+   resolved the loops against. */
+static int g_threads = 0;
+
 static int bad_args(const double* const* partials, int n_parts,
                     const double* residual, const double* weight,
                     double* const* out, int n_out, double* residual_out,
@@ -96,7 +101,7 @@ int tw_oracle_traditional(const double* const* partials, int n_parts,
      * tokens of the range (§1: the reduced tensor is [T, H] on every GPU). */
     double* reduced = (double*)malloc((size_t)(n_rows * H) * sizeof(double));
     if (!reduced) return -1;
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(tw_oracle_threads())
     for (int64_t i = 0; i < n_rows; ++i) {
         const int64_t t = t0 + i;
         for (int64_t h = 0; h < H; ++h) {
@@ -110,7 +115,7 @@ int tw_oracle_traditional(const double* const* partials, int n_parts,
     /* Step 2, on each rank k (the redundant N-fold work of §1): residual add,
      * then RMSNorm of every token, into that rank's own destination. */
     for (int k = 0; k < n_out; ++k) {
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(tw_oracle_threads())
         for (int64_t i = 0; i < n_rows; ++i) {
             const int64_t t = t0 + i;
             double* x = (double*)malloc((size_t)H * sizeof(double));
@@ -149,7 +154,7 @@ int tw_oracle_reordered(const double* const* partials, int n_parts,
 
         /* ReduceScatter on token boundaries (§3.2): rank r receives the
          * sum over all ranks of its own token slice, full feature width. */
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(tw_oracle_threads())
         for (int64_t i = 0; i < n_mine; ++i) {
             const int64_t t = t0 + first + i;
             for (int64_t h = 0; h < H; ++h) {
@@ -162,7 +167,7 @@ int tw_oracle_reordered(const double* const* partials, int n_parts,
 
         /* Residual add on the slice only, then RMSNorm (§3.3).  The
          * normalised slice overwrites the reduced one in place per token. */
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(tw_oracle_threads())
         for (int64_t i = 0; i < n_mine; ++i) {
             const int64_t t = t0 + first + i;
             double* row = mine + i * H;
@@ -188,7 +193,7 @@ int tw_oracle_reordered(const double* const* partials, int n_parts,
 int tw_oracle_threads(void)
 {
 #ifdef _OPENMP
-    return omp_get_max_threads();
+    return g_threads > 0 ? g_threads : omp_get_max_threads();
 #else
     return 1;
 #endif
@@ -196,10 +201,6 @@ int tw_oracle_threads(void)
 
 void tw_oracle_set_threads(int n)
 {
-#ifdef _OPENMP
     if (n >= 1)
-        omp_set_num_threads(n);
-#else
-    (void)n;
-#endif
+        g_threads = n;
 }

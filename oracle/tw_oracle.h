@@ -58,8 +58,8 @@ int tw_oracle_token_slice(int64_t n_tokens, int n_ranks, int r,
 /* Number of threads the oracle's token loops use (1 without OpenMP). */
 int tw_oracle_threads(void);
 
-/* Sets the thread count for later calls from the calling thread (n >= 1;
-   other values are ignored).  Overrides OMP_NUM_THREADS. */
+/* Sets the thread count of later calls (n >= 1; other values are ignored).
+   Overrides OMP_NUM_THREADS. */
 void tw_oracle_set_threads(int n);
 
 #ifdef __cplusplus

@@ -71,6 +71,7 @@ BUDGET_SHAPES = [
     wl(3, 11, 16384),                  # 4 vectors per thread
     wl(6, 19, 4096, "f32", n_out=3),
     wl(3, 27, 1000),                   # ragged row, one vector per thread
+    wl(16, 3000, 64, n_out=2),         # 16 one-token stages: the ring wraps ~190 times per CTA
 ]
 
 

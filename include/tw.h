@@ -49,7 +49,8 @@
  *   - Argument rules, checked on the host before any CUDA call:
  *       partials/out arrays and every pointer in them non-NULL;
  *       1 <= n_parts <= TW_MAX_PARTS, 1 <= n_out <= TW_MAX_OUTS;
- *       T >= 0, 1 <= H <= TW_MAX_H(dtype), 0 <= t0 <= t1 <= T;
+ *       T >= 0, 1 <= H <= TW_MAX_H(dtype), 0 <= t0 <= t1 <= T, and a
+ *       buffer's T*H*size bytes fit in 2^48 (a device address range);
  *       eps finite and >= 0; max_sms >= 1 (values above the SM count clamp);
  *       H * sizeof(dtype) a multiple of 16 and every pointer 16-byte aligned
  *       (else TW_ERR_ALIGNMENT);

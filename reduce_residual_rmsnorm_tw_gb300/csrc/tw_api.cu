@@ -152,6 +152,11 @@ int check_args(const Args& a) {
     if (a.H > max_h)
         return fail(TW_ERR_UNSUPPORTED, "H %lld above the limit %lld for this dtype",
                     (long long)a.H, (long long)max_h);
+    // A buffer's byte span must be a plausible device address range, so that
+    // T * H * size and every pointer + offset below stay far from overflow.
+    if (a.T > (int64_t{1} << 48) / (a.H * static_cast<int64_t>(elem_size(a.dtype))))
+        return fail(TW_ERR_INVALID_ARG, "T %lld x H %lld buffers exceed 2^48 bytes",
+                    (long long)a.T, (long long)a.H);
     if (a.t0 < 0 || a.t0 > a.t1 || a.t1 > a.T)
         return fail(TW_ERR_INVALID_ARG, "token range [%lld, %lld) not within [0, %lld]",
                     (long long)a.t0, (long long)a.t1, (long long)a.T);

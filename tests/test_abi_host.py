@@ -81,6 +81,7 @@ def call(lib, n_parts=2, n_out=1, T=4, H=64, eps=1e-6, t0=0, t1=None,
     ({"H": 6, "dtype": 1}, ALIGN),            # 24 bytes per row
     ({"residual": BASE + 64 * MB + 8}, ALIGN),
     ({"partials": [BASE, BASE + MB + 4]}, ALIGN),
+    ({"T": 1 << 47, "t1": 1}, INVALID),       # buffers of 2^54 bytes: over 2^48
     ({"H": 16392}, UNSUP),                    # above the bf16 limit
     ({"H": 8196, "dtype": 1}, UNSUP),         # above the fp32 limit
     ({"residual_out": BASE + 64 * MB + 16}, ALIAS),   # overlaps residual, not equal

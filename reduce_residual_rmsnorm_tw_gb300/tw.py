@@ -68,6 +68,10 @@ def load():
         pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64, ctypes.c_float,
         i64, i64, ctypes.c_int, vp, ctypes.c_size_t, i64, vp, ctypes.c_int]
     lib.tw_fused_reduce_add_rmsnorm_host.restype = ctypes.c_int
+    lib.tw_fused_reduce_add_rmsnorm_host_noalloc.argtypes = [
+        pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64, ctypes.c_float,
+        i64, i64, ctypes.c_int, i64, vp, ctypes.c_int]
+    lib.tw_fused_reduce_add_rmsnorm_host_noalloc.restype = ctypes.c_int
     lib.tw_host_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64,
                                             ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     lib.tw_host_workspace_bytes.restype = ctypes.c_int
@@ -94,8 +98,10 @@ def _stream_handle(stream):
     return stream.cuda_stream
 
 
-def _marshal(partials, residual, weight, out, residual_out):
-    """Pointer arrays and (T, H, dtype) from tensors; shapes must agree."""
+def _marshal(partials, residual, weight, out, residual_out, on_device=True):
+    """Pointer arrays and (T, H, dtype) from tensors; shapes must agree.  The
+    device entry points take tensors on the current CUDA device; the host
+    entry points (on_device=False) take pinned CPU tensors."""
     partials, out = list(partials), list(out)
     if not partials or not out:
         raise ValueError("need at least one partial and one destination")
@@ -114,6 +120,15 @@ def _marshal(partials, residual, weight, out, residual_out):
     if (weight.shape != (H,) or weight.dtype != dtype
             or not weight.is_contiguous()):
         raise ValueError(f"weight must be a contiguous [{H}] {dtype} tensor")
+    every = partials + out + [residual, weight, residual_out]
+    if on_device:
+        if any(not t.is_cuda for t in every):
+            raise ValueError("every tensor must be on the current CUDA device")
+        dev = torch.cuda.current_device()
+        if any(t.device.index != dev for t in every):
+            raise ValueError(f"every tensor must be on the current CUDA device (cuda:{dev})")
+    elif any(t.is_cuda or not t.is_pinned() for t in every):
+        raise ValueError("every tensor must be a pinned (page-locked) CPU tensor")
     p_arr = (ctypes.c_void_p * len(partials))(*[t.data_ptr() for t in partials])
     o_arr = (ctypes.c_void_p * len(out))(*[t.data_ptr() for t in out])
     return p_arr, len(partials), o_arr, len(out), T, H, _DTYPES[dtype]
@@ -124,7 +139,7 @@ def tw_fused_reduce_add_rmsnorm_ex(partials, residual, weight, out,
                                    max_sms=None, stream=None, path="auto",
                                    smid_log=None):
     """Fused reduce + residual add + RMSNorm on rows [t0, t1), kernel chosen
-    by ``path`` ("auto", "rows" or "warp").  ``smid_log`` is an optional int32
+    by ``path`` ("auto", "rows", "warp" or "cluster").  ``smid_log`` is an optional int32
     device tensor with at least max_sms entries."""
     p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
                                                 out, residual_out)
@@ -235,7 +250,9 @@ def tw_fused_reduce_add_rmsnorm_host(partials, residual, weight, out,
     ``chunk_tokens`` tokens through the device ``workspace`` (a uint8 CUDA
     tensor of at least tw_host_workspace_bytes bytes)."""
     p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
-                                                out, residual_out)
+                                                out, residual_out, on_device=False)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
     rc = load().tw_fused_reduce_add_rmsnorm_host(
         p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
         residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
@@ -252,16 +269,9 @@ def tw_fused_reduce_add_rmsnorm_host_noalloc(partials, residual, weight, out,
     """The host-buffer step for callers that cannot allocate device memory:
     pinned host tensors only; the library stages the chunks in its own
     fixed device array (chunk_tokens <= 0: the largest chunk that fits)."""
-    lib = load()
-    fn = lib.tw_fused_reduce_add_rmsnorm_host_noalloc
-    vp, i64 = ctypes.c_void_p, ctypes.c_int64
-    pp = ctypes.POINTER(ctypes.c_void_p)
-    fn.argtypes = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int, vp, i64, i64,
-                   ctypes.c_float, i64, i64, ctypes.c_int, i64, vp, ctypes.c_int]
-    fn.restype = ctypes.c_int
     p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
-                                                out, residual_out)
-    rc = fn(p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
+                                                out, residual_out, on_device=False)
+    rc = load().tw_fused_reduce_add_rmsnorm_host_noalloc(p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
             residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
             _ALL_SMS if max_sms is None else max_sms, chunk_tokens,
             _stream_handle(stream), dt)

@@ -139,6 +139,13 @@ def test_binding_marshalling_checks():
     with pytest.raises(ValueError):
         tw.tw_fused_reduce_add_rmsnorm_f32([x], x, torch.zeros(64, dtype=torch.bfloat16),
                                            [x.clone()], x.clone(), 1e-6)
+    # Well-formed CPU tensors: refused for a device entry point before any
+    # CUDA call, and unpinned ones for a host entry point.
+    w = torch.zeros(64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        tw.tw_fused_reduce_add_rmsnorm([x], x, w, [x.clone()], x.clone(), 1e-6)
+    with pytest.raises(ValueError, match="pinned"):
+        tw.tw_fused_reduce_add_rmsnorm_host_noalloc([x], x, w, [x.clone()], x.clone(), 1e-6)
 
 
 def test_colsplit_slice_alignment(lib):

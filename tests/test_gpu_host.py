@@ -2,6 +2,7 @@
 token range pipelined in chunks.  Checked against the oracle element by
 element, and bit for bit against the device entry point when every chunk
 runs on the same kernel."""
+import ctypes
 from dataclasses import replace
 
 import pytest
@@ -68,11 +69,29 @@ def test_host_rejects_pageable_memory():
     wl = CASES[0].with_tokens(4)
     d = inputs.make_inputs(wl)
     out = [torch.empty(4, wl.H, dtype=wl.torch_dtype)]
-    ws = torch.empty(tw.tw_host_workspace_bytes(8, 1, wl.H, 4, wl.torch_dtype),
-                     dtype=torch.uint8, device="cuda")
-    with pytest.raises(tw.TwError, match="page-locked"):
+    res_out = torch.empty_like(out[0])
+    nbytes = tw.tw_host_workspace_bytes(8, 1, wl.H, 4, wl.torch_dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    # The binding refuses pageable tensors before the call ...
+    with pytest.raises(ValueError, match="pinned"):
         tw.tw_fused_reduce_add_rmsnorm_host(d["partials"], d["residual"], d["weight"], out,
-                                            torch.empty_like(out[0]), wl.eps, ws, 4)
+                                            res_out, wl.eps, ws, 4)
+    # ... and so does the C entry point when called with their addresses.
+    ptrs = lambda ts: (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])  # noqa: E731
+    rc = tw.load().tw_fused_reduce_add_rmsnorm_host(
+        ptrs(d["partials"]), 8, d["residual"].data_ptr(), d["weight"].data_ptr(), ptrs(out), 1,
+        res_out.data_ptr(), 4, wl.H, wl.eps, 0, 4, 1 << 30, ws.data_ptr(), nbytes, 4,
+        torch.cuda.current_stream().cuda_stream, tw.TW_BF16)
+    assert rc == -1 and "page-locked" in tw.tw_last_error_string()
+
+
+def test_binding_refuses_tensors_off_the_device():
+    wl = CASES[0].with_tokens(4)
+    d = inputs.make_inputs(wl)   # CPU tensors
+    out = [torch.empty(4, wl.H, dtype=wl.torch_dtype)]
+    with pytest.raises(ValueError, match="current CUDA device"):
+        tw.tw_fused_reduce_add_rmsnorm(d["partials"], d["residual"], d["weight"], out,
+                                       torch.empty_like(out[0]), wl.eps)
 
 
 def test_host_in_place_residual():

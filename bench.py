@@ -72,14 +72,40 @@ def measured_peaks():
 ROWS_KERNEL_SOURCES = ("tw_api.cu", "tw_device.cuh", "tw_internal.h", "tw_rows.cu")
 
 
+def code_only(text):
+    """C/C++ source without comments and whitespace (string and character
+    literals kept), so that edits to comments leave the hash unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            i = text.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash():
-    """Hash of the rows kernel's sources: a stored ncu traffic figure is only
-    reported while it still describes the kernel being timed."""
+    """Hash of the rows kernel's code (comments and whitespace left out): a
+    stored ncu traffic figure is only reported while it still describes the
+    kernel being timed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_tw_gb300", "csrc")
     for name in ROWS_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + b"\0" + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

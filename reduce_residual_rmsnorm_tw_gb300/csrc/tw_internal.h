@@ -14,7 +14,7 @@ constexpr int kRowsThreads = 512;
 constexpr int kRowsMaxVecs = 4;
 // Producer warps of the rows kernel (one elected lane each issues the bulk
 // copies of the ring stages it owns).  One SM's copy rate grows with the
-// number of threads issuing copies, so a CTA that streams alone on its SM
+// number of warps issuing copies, so a CTA that streams alone on its SM
 // issues from several.
 constexpr int kRowsMaxProducers = 2;
 // Target bytes of one ring stage of the rows kernel (whole input rows of one

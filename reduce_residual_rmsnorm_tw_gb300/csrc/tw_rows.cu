@@ -17,8 +17,8 @@
 // (transaction bytes) and an "empty" mbarrier (one arrival per consumer
 // warp).  The ring's stages are dealt round robin to `producers` warps (one
 // elected lane each): the copy rate of one SM grows with the number of
-// threads issuing copies (one issuing thread streamed ~36 GB/s of 16 KB
-// copies whatever the ring depth, two ~69 GB/s), which is what bounds a CTA
+// warps issuing copies (one issuing warp streamed ~36 GB/s of 16 KB copies
+// whatever the ring depth, two ~69 GB/s), which is what bounds a CTA
 // streaming alone on its SM under a small SM budget.  Whole-row copies keep
 // several large copies from different buffers in flight.  The 512 consumer
 // threads own the 16-byte vectors tid, tid + 512, ... of the row: they add the

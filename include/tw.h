@@ -186,7 +186,10 @@ int tw_fused_reduce_add_rmsnorm_flags(const void* const* partials, int n_parts,
 /* Two-chunk token split ("Der intelligente Split"): rows [0, t_split) run on
  * stream s0 and rows [t_split, T) on stream s1, each a rows-kernel launch with
  * its own budget of max_sms SMs (so up to 2*max_sms SMs while both run).
- * t_split < 0 picks T/2.  s1 first waits for work already queued on s0, and
+ * t_split < 0 picks T/2 moved to the nearest multiple of the first chunk's
+ * grid, min(max_sms, SM count), when T is at least twice that (whole waves of
+ * one token per CTA; the result does not depend on the split point).  s1
+ * first waits for work already queued on s0, and
  * s0 is made to wait for the s1 chunk, so synchronising s0 alone covers both
  * chunks.  Same argument rules as above, with t_split <= T. */
 int tw_split_launch(const void* const* partials, int n_parts,

@@ -472,13 +472,21 @@ int tw_split_launch(const void* const* partials, int n_parts, const void* residu
                  T,        H,       eps,      0,      T,   max_sms, dtype};
     int rc = tw::check_args(a);
     if (rc != TW_OK) return rc;
-    if (t_split < 0) t_split = T / 2;
     if (t_split > T)
         return tw::fail(TW_ERR_INVALID_ARG, "t_split %lld > T %lld", (long long)t_split,
                         (long long)T);
     if (T == 0) return TW_OK;
     tw::DeviceState* d = nullptr;
     if ((rc = tw::device_state(&d)) != TW_OK) return rc;
+    if (t_split < 0) {
+        // Wave-aware default ("Der intelligente Split" names the idea, no
+        // formula): T/2 moved to the nearest whole number of waves of the
+        // first chunk's grid (one token per CTA per wave), so that chunk
+        // ends without a partial last wave.
+        const int64_t w = max_sms < d->sm_count ? max_sms : d->sm_count;
+        t_split = T / 2;
+        if (T >= 2 * w) t_split = (T / 2 + w / 2) / w * w;
+    }
 
     cudaStream_t st0 = static_cast<cudaStream_t>(s0), st1 = static_cast<cudaStream_t>(s1);
     std::lock_guard<std::mutex> lock(d->split_mu);

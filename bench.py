@@ -67,9 +67,10 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-# The sources that define the timed rows-kernel launch: the kernel, its
-# device helpers and parameters, and the host code that sizes and launches it.
-ROWS_KERNEL_SOURCES = ("tw_api.cu", "tw_device.cuh", "tw_internal.h", "tw_rows.cu")
+# The sources that define the timed rows-kernel launch: the kernel with its
+# launch plan (stage sizes, ring depth, producers), its device helpers and
+# its parameters.
+ROWS_KERNEL_SOURCES = ("tw_device.cuh", "tw_internal.h", "tw_rows.cu")
 
 
 def code_only(text):

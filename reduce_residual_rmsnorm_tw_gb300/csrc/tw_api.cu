@@ -260,36 +260,10 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 
     int err;
     if (path == TW_PATH_ROWS) {
-        // Whole input rows of one token per stage: the whole token if its R
-        // rows fit kStageTargetBytes, else the token's rows split evenly over
-        // the fewest stages that fit (never more than R rows).  As many
-        // stages as fit the shared memory.
-        const int64_t rows = a.colsplit ? 2 : a.n_parts + 1;
-        const int64_t parts = (rows * p.row_bytes + kStageTargetBytes - 1) / kStageTargetBytes;
-        int64_t per_stage = (rows + parts - 1) / parts;
-        if (per_stage * p.row_bytes > kStageTargetBytes)
-            per_stage = kStageTargetBytes / p.row_bytes;
-        if (per_stage < 1) per_stage = 1;
-        p.rows_per_stage = static_cast<int>(per_stage);
-        const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);
-        int stages = static_cast<int>(
-            (static_cast<size_t>(d.smem_optin) - rows_smem_bytes(0, 0)) / stage);
-        if (stages > kMaxStages) stages = kMaxStages;
-        if (stages < kMinStages)
+        const size_t smem = rows_plan(p, d.smem_optin);
+        if (smem == 0)
             return fail(TW_ERR_UNSUPPORTED, "shared memory too small for rows of %lld bytes",
                         (long long)p.row_bytes);
-        // Producer warps: the largest power of two up to kRowsMaxProducers
-        // that the ring holds; the ring is cut to a multiple of it, so each
-        // producer owns the same stages for the whole launch.
-        static_assert((kRowsMaxProducers & (kRowsMaxProducers - 1)) == 0,
-                      "producer count must be a power of two");
-        int producers = kRowsMaxProducers;
-        while (producers > 1 && producers > stages) producers /= 2;
-        stages -= stages % producers;
-        p.stages = stages;
-        p.producers = producers;
-        size_t smem = rows_smem_bytes(stage, stages);
-        if (smem < static_cast<size_t>(kExclusiveSmemBytes)) smem = kExclusiveSmemBytes;
         const int grid = static_cast<int>(tokens < sms ? tokens : sms);
         err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
     } else if (path == TW_PATH_WARP) {

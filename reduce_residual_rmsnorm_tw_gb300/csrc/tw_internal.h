@@ -77,6 +77,10 @@ int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pd
                 void* stream);
 // Shared memory of the rows kernel for a stage size and ring depth.
 size_t rows_smem_bytes(size_t stage_bytes, int stages);
+// Launch plan of the rows kernel for p (row_bytes, n_parts and colsplit set):
+// sets rows_per_stage, stages and producers and returns the dynamic shared
+// memory to request, or 0 if the rows do not fit in smem_optin bytes.
+size_t rows_plan(Params& p, int smem_optin);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).
 int rows_set_smem_limit(int smem_optin);

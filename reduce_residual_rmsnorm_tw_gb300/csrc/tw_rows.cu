@@ -337,6 +337,35 @@ size_t rows_smem_bytes(size_t stage_bytes, int stages) {
     return static_cast<size_t>(kRingOff) + static_cast<size_t>(stages) * stage_bytes;
 }
 
+size_t rows_plan(Params& p, int smem_optin) {
+    // Whole input rows of one token per stage: the whole token if its R rows
+    // fit kStageTargetBytes, else the token's rows split evenly over the
+    // fewest stages that fit (never more than R rows).  As many stages as fit
+    // the shared memory.
+    const int64_t rows = p.colsplit ? 2 : p.n_parts + 1;
+    const int64_t parts = (rows * p.row_bytes + kStageTargetBytes - 1) / kStageTargetBytes;
+    int64_t per_stage = (rows + parts - 1) / parts;
+    if (per_stage * p.row_bytes > kStageTargetBytes) per_stage = kStageTargetBytes / p.row_bytes;
+    if (per_stage < 1) per_stage = 1;
+    const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);
+    int stages = static_cast<int>((static_cast<size_t>(smem_optin) - rows_smem_bytes(0, 0)) / stage);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < kMinStages) return 0;
+    // Producer warps: the largest power of two up to kRowsMaxProducers that
+    // the ring holds; the ring is cut to a multiple of it, so each producer
+    // owns the same stages for the whole launch.
+    static_assert((kRowsMaxProducers & (kRowsMaxProducers - 1)) == 0,
+                  "producer count must be a power of two");
+    int producers = kRowsMaxProducers;
+    while (producers > 1 && producers > stages) producers /= 2;
+    stages -= stages % producers;
+    p.rows_per_stage = static_cast<int>(per_stage);
+    p.stages = stages;
+    p.producers = producers;
+    const size_t smem = rows_smem_bytes(stage, stages);
+    return smem < static_cast<size_t>(kExclusiveSmemBytes) ? kExclusiveSmemBytes : smem;
+}
+
 int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
         for (int nv = 1; nv <= kRowsMaxVecs; ++nv) {

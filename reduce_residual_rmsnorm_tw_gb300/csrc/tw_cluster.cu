@@ -9,9 +9,11 @@
 // The C CTAs of a cluster split the token's columns into C contiguous slices.
 // Each thread issues all N + 1 loads of its vectors at once, sums them, and
 // the CTA's partial sum of squares is exchanged through distributed shared
-// memory: every CTA publishes its total in its own shared memory, one cluster
-// barrier makes them visible, and every thread adds the C totals in rank order
-// (so all CTAs get the same bits).  No global scratch and no multicast.
+// memory: every CTA writes its total into the shared memory of every CTA of
+// the cluster, one cluster barrier makes them visible, and every thread adds
+// the C totals in rank order from its own shared memory (so all CTAs get the
+// same bits, and no CTA reads a peer's memory, so none has to wait for its
+// peers before leaving).  No global scratch and no multicast.
 #include "tw_device.cuh"
 
 namespace tw {
@@ -43,16 +45,21 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// Cluster barrier in two halves: arrive (no ordering) early, wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// Write a float into the shared memory of CTA `rank` of this cluster, at the
 // same offset as `local` in this CTA.
-__device__ __forceinline__ float ld_peer_f32(const float* local, uint32_t rank) {
+__device__ __forceinline__ void st_peer_f32(float* local, uint32_t rank, float v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                  : "=r"(remote)
                  : "r"(smem_addr(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 template <typename T, int VPT>
@@ -62,7 +69,9 @@ __global__ void __launch_bounds__(kClusterThreads)
     constexpr int E = V::kElems;
     constexpr int kWarps = kClusterThreads / 32;
     __shared__ float warp_part[kWarps];
-    __shared__ float cta_part[2];
+    // cta_part[b][r]: CTA r's sum of squares of the token using buffer b,
+    // written into every CTA of the cluster by CTA r itself.
+    __shared__ float cta_part[2][kClusterMaxSize];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -86,9 +95,14 @@ __global__ void __launch_bounds__(kClusterThreads)
             bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, bytes);
         }
     }
+    // Every CTA of the cluster must be running before any writes into its
+    // shared memory: arrive now, wait just before the first such write (the
+    // global loads of the first token hide the wait).
+    cluster_arrive_relaxed();
     grid_dependency_wait();
     grid_launch_dependents();
     if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
+    bool peers_started = false;
 
     uint4 wv[VPT];
 #pragma unroll
@@ -139,15 +153,24 @@ __global__ void __launch_bounds__(kClusterThreads)
         ss = warp_sum(ss);
         if (lane == 0) warp_part[warp] = ss;
         __syncthreads();
-        if (tid == 0) {
+        if (!peers_started) {
+            cluster_wait();
+            peers_started = true;
+        }
+        // Thread r < C pushes this CTA's total into CTA r; after the barrier
+        // every CTA holds all C totals locally and adds them in rank order
+        // (the same bits everywhere).  A peer writes buffer `buf` again only
+        // two tokens later, after the barrier of the next token, which this
+        // CTA reaches only once it has read this one.
+        if (tid < static_cast<int>(csize)) {
             float s = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) s += warp_part[w];
-            cta_part[buf] = s;
+            st_peer_f32(&cta_part[buf][crank], static_cast<uint32_t>(tid), s);
         }
         cluster_sync();
         float total = 0.f;
-        for (uint32_t r = 0; r < csize; ++r) total += ld_peer_f32(&cta_part[buf], r);
+        for (uint32_t r = 0; r < csize; ++r) total += cta_part[buf][r];
         buf ^= 1;
         const float inv = rsqrtf(total * p.inv_H + p.eps);
 
@@ -167,8 +190,10 @@ __global__ void __launch_bounds__(kClusterThreads)
             }
         }
     }
-    // No CTA may leave while a peer can still read its shared memory.
-    cluster_sync();
+    // A CTA with no token still completes the start-up barrier; after the
+    // last token's barrier no CTA touches another's shared memory, so each
+    // leaves as soon as its own stores are issued.
+    if (!peers_started) cluster_wait();
 }
 
 template <typename T>

@@ -29,6 +29,7 @@ CASES = [
     wl(5, 21, 8192, "f32"),            # max fp32 H
     wl(16, 7, 1028, "f32", n_out=2),   # ragged fp32 chunk
     wl(3, 40, 6000, "f32", eps=0.5),   # large eps, 6 ragged chunks
+    wl(4, 23, 2048, eps=0.0),          # eps = 0 (rows are never all zero)
 ]
 
 

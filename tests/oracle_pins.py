@@ -208,6 +208,29 @@ def pin_bad_arguments(orc):
         raise AssertionError("accepted eps < 0")
 
 
+def pin_special_values(orc):
+    """IEEE special values follow from the definition with no special case: a
+    NaN element makes its token's rms NaN (every y of the token NaN,
+    residual_out NaN there only); an infinite element makes the rms infinite
+    (y NaN there, x / inf = 0 elsewhere in the row); other tokens are finite.
+    Both orders agree on the pattern."""
+    rng = np.random.default_rng(13)
+    T, H, N = 4, 16, 3
+    parts = [rng.standard_normal((T, H)) for _ in range(N)]
+    residual = rng.standard_normal((T, H))
+    w = rng.uniform(0.5, 1.5, H)
+    parts[1][1, 3] = math.nan
+    parts[0][2, 7] = math.inf
+    for fn in (orc.reordered, orc.traditional):
+        out, res = fn(parts, residual, w, 1e-6)
+        y = out[0]
+        assert np.isnan(y[1]).all() and np.isnan(res[1, 3])
+        assert np.isfinite(np.delete(res[1], 3)).all()
+        assert np.isnan(y[2, 7]) and np.isposinf(res[2, 7])
+        assert (np.delete(y[2], 7) == 0.0).all()
+        assert np.isfinite(y[[0, 3]]).all() and np.isfinite(res[[0, 3]]).all()
+
+
 PINS = [pin_hidden4_example, pin_eps_inside_sqrt, pin_library_rms_norm,
         pin_unit_rms, pin_order_equivalence, pin_shape_walkthrough,
-        pin_zero_pad_concat, pin_invariants, pin_bad_arguments]
+        pin_zero_pad_concat, pin_invariants, pin_bad_arguments, pin_special_values]

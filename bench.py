@@ -503,9 +503,42 @@ def sweep(args, sync_ranks):
         str(b): entry(wl, device_leg(res, 3 if b <= 4 else 20, 2, max_sms=b)["mean_launch_ms"])
         for b in (2, 4, 8, 16, 148)}
     del res
+    out["flags_raised:" + HEADLINE] = flags_leg(W[HEADLINE], steps)
     out["unfused_torch_chain"] = unfused_leg(W[HEADLINE], steps)
     out["oracle_threads"] = {str(n): cpu_baseline(W[HEADLINE], 5.0, threads=n)
                              for n in (1, host_cores())}
+    return out
+
+
+def flags_leg(wl, steps):
+    """The readiness-flag entry point with every flag already raised (one
+    flag per token, and one per 64 tokens) against the plain launch: the cost
+    of checking the flags, and of giving up the L2 warming that flag launches
+    do not do (their rows may not exist before the flag)."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import tw
+    res = Resident(wl)
+    peak, _ = measured_peaks()
+    stream = torch.cuda.Stream()
+    out = {}
+
+    def entry(ms):
+        gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
+        return {"launch_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                "frac_of_measured_hbm": round(gbs / peak, 4)}
+
+    region, _ = time_launches(res.launchers(), steps, 20, stream)
+    out["plain"] = entry(region / steps)
+    for bt in (1, 64):
+        ready = torch.ones(-(-res.big.T // bt), dtype=torch.int32, device="cuda")
+        launchers = [tw.prepare(res.partials, res.residual, res.weight, res.out,
+                                res.residual_out, wl.eps, t0, t1, ready=ready,
+                                block_tokens=bt, epoch=1) for t0, t1 in res.ranges()]
+        region, _ = time_launches(launchers, steps, 20, stream)
+        out[f"flags_block_{bt}"] = entry(region / steps)
+    check_status()
+    del res
+    torch.cuda.empty_cache()
     return out
 
 

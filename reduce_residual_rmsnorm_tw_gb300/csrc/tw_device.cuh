@@ -80,6 +80,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// One acquire read of a readiness flag: has *flag reached `epoch` (compared
+// wrap-safe as a signed difference)?
+__device__ __forceinline__ bool flag_is_ready(const unsigned int* flag, unsigned int epoch) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return static_cast<int>(v - epoch) >= 0;
+}
+
 // Wait until *flag has reached `epoch` (compared wrap-safe as a signed
 // difference), reading with acquire semantics at GPU scope, then order the
 // async proxy (bulk copies) after it.  Returns false after kWaitLimitNs or

@@ -96,7 +96,9 @@ struct RingPos {
 
 constexpr int kRowsBlock = kRowsThreads + 32 * kRowsMaxProducers;
 
-template <typename T, int NV>
+// FLAGS: the readiness-flag variant (p.ready set).  A separate instantiation,
+// so the plain kernel carries no flag code at all.
+template <typename T, int NV, bool FLAGS>
 __global__ void __launch_bounds__(kRowsBlock, 1)
     rows_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -130,11 +132,13 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     }
     __syncthreads();
     // While the previous kernel of the stream drains (launches that may
-    // overlap it only), warm L2 with this CTA's first tokens.  A prefetch only fills L2, which is where every write of
-    // that kernel lands too, so data read after the wait below is current even
-    // if the previous kernel writes these rows.  (Not with readiness flags:
-    // their rows may not exist yet.)
-    if (warp == kConsumerWarps && lane == 0 && p.prefetch && !p.ready) {
+    // overlap it only), warm L2 with this CTA's first tokens.  A prefetch only
+    // fills L2, which is where every write of that kernel lands too, so data
+    // read after the wait below is current even if the previous kernel writes
+    // these rows.  With readiness flags only rows whose flag is already up
+    // are warmed (a raised flag means its rows are final); the first token
+    // whose flag is not up ends the warming.
+    if (warp == kConsumerWarps && lane == 0 && p.prefetch) {
         const int64_t t_first = p.t0 + blockIdx.x;
         const int64_t token_bytes = static_cast<int64_t>(R) * rb;
         int64_t n_pre = kPrefetchTokens;
@@ -142,6 +146,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         for (int64_t i = 0; i < n_pre; ++i) {
             const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;
             if (t >= p.t1) break;
+            if (FLAGS && !flag_is_ready(p.ready + t / p.block_tokens, p.epoch)) break;
             prefetch_token(p, t, R, n_sum);
         }
     }
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
                 const uint32_t s = pos.stage;
                 if ((s & (P - 1)) != pw) continue;
-                if (p.ready) {
+                if (FLAGS) {
                     const int64_t b = t / p.block_tokens;
                     if (b != ready_block) {
                         if (!flag_wait(p.ready + b, p.epoch, abort_flag)) {
@@ -312,19 +317,22 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     }
 }
 
-template <typename T>
+template <typename T, bool FLAGS>
 void* rows_entry_for(int nv) {
     switch (nv) {
-        case 1: return reinterpret_cast<void*>(&rows_kernel<T, 1>);
-        case 2: return reinterpret_cast<void*>(&rows_kernel<T, 2>);
-        case 3: return reinterpret_cast<void*>(&rows_kernel<T, 3>);
-        case 4: return reinterpret_cast<void*>(&rows_kernel<T, 4>);
+        case 1: return reinterpret_cast<void*>(&rows_kernel<T, 1, FLAGS>);
+        case 2: return reinterpret_cast<void*>(&rows_kernel<T, 2, FLAGS>);
+        case 3: return reinterpret_cast<void*>(&rows_kernel<T, 3, FLAGS>);
+        case 4: return reinterpret_cast<void*>(&rows_kernel<T, 4, FLAGS>);
         default: return nullptr;
     }
 }
 
-void* rows_kernel_for(int dtype, int nv) {
-    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nv) : rows_entry_for<float>(nv);
+void* rows_kernel_for(int dtype, int nv, bool flags) {
+    if (dtype == TW_BF16)
+        return flags ? rows_entry_for<__nv_bfloat16, true>(nv)
+                     : rows_entry_for<__nv_bfloat16, false>(nv);
+    return flags ? rows_entry_for<float, true>(nv) : rows_entry_for<float, false>(nv);
 }
 
 int rows_vectors_per_thread(int64_t row_bytes) {
@@ -368,18 +376,19 @@ size_t rows_plan(Params& p, int smem_optin) {
 
 int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
-        for (int nv = 1; nv <= kRowsMaxVecs; ++nv) {
-            cudaError_t e = cudaFuncSetAttribute(rows_kernel_for(dt, nv),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 smem_optin);
-            if (e != cudaSuccess) return static_cast<int>(e);
-        }
+        for (int nv = 1; nv <= kRowsMaxVecs; ++nv)
+            for (bool flags : {false, true}) {
+                cudaError_t e = cudaFuncSetAttribute(rows_kernel_for(dt, nv, flags),
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     smem_optin);
+                if (e != cudaSuccess) return static_cast<int>(e);
+            }
     return 0;
 }
 
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream) {
-    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes));
+    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.ready != nullptr);
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
     return launch_with_pdl(fn, p, grid, kRowsBlock, smem_bytes, pdl, stream);
 }

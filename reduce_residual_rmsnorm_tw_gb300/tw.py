@@ -300,7 +300,7 @@ class Prepared:
     kernel.  The tensors must stay alive and unchanged in shape."""
 
     def __init__(self, partials, residual, weight, out, residual_out, eps, t0=0,
-                 t1=None, max_sms=None, path="auto"):
+                 t1=None, max_sms=None, path="auto", ready=None, block_tokens=0, epoch=0):
         p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
                                                     out, residual_out)
         self._keep = (p_arr, o_arr, list(partials), residual, weight, list(out),
@@ -309,7 +309,14 @@ class Prepared:
                       n_out, residual_out.data_ptr(), T, H, eps, t0,
                       T if t1 is None else t1,
                       _ALL_SMS if max_sms is None else max_sms]
-        if path == "colsplit":
+        if ready is not None:
+            # tw_fused_reduce_add_rmsnorm_flags: gated by readiness flags.
+            if ready.dtype != torch.int32 or not ready.is_cuda:
+                raise ValueError("ready must be an int32 CUDA tensor")
+            self._keep += (ready,)
+            self._fn = load().tw_fused_reduce_add_rmsnorm_flags
+            self._tail = [dt, ready.data_ptr(), block_tokens, epoch & 0xFFFFFFFF]
+        elif path == "colsplit":
             # tw_fused_reduce_add_rmsnorm_colsplit: zero-padded column split.
             self._fn = load().tw_fused_reduce_add_rmsnorm_colsplit
             self._tail = [dt]
@@ -325,9 +332,10 @@ class Prepared:
 
 
 def prepare(partials, residual, weight, out, residual_out, eps, t0=0, t1=None,
-            max_sms=None, path="auto"):
+            max_sms=None, path="auto", ready=None, block_tokens=0, epoch=0):
     """Marshal a fused call once; returns a :class:`Prepared` callable.
     ``path`` is a kernel name of tw_fused_reduce_add_rmsnorm_ex, or "colsplit"
-    for tw_fused_reduce_add_rmsnorm_colsplit."""
+    for tw_fused_reduce_add_rmsnorm_colsplit; with ``ready`` the call is
+    tw_fused_reduce_add_rmsnorm_flags."""
     return Prepared(partials, residual, weight, out, residual_out, eps, t0, t1,
-                    max_sms, path)
+                    max_sms, path, ready, block_tokens, epoch)

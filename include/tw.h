@@ -95,8 +95,8 @@ typedef enum {
 
 /* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
 typedef enum {
-    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 16 tokens,
-                          rows kernel otherwise */
+    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 8 tokens (when
+                          the row fits a cluster), rows kernel otherwise */
     TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
                           staged into shared memory by bulk async copies */
     TW_PATH_WARP = 2,  /* one warp per token, no shared memory */
@@ -133,9 +133,10 @@ int tw_fused_reduce_add_rmsnorm(const void* const* partials, int n_parts,
                                 int dtype);
 
 /* Same, with the kernel chosen explicitly (tw_path).  smid_log, when not NULL,
- * is a DEVICE array of at least max_sms uint32 entries; every CTA of the rows
- * kernel writes the id of the SM it ran on to smid_log[blockIdx.x] (used to
- * check the SM budget; entries of CTAs not launched are left alone). */
+ * is a DEVICE array of at least max_sms uint32 entries; every CTA of the
+ * launched kernel writes the id of the SM it ran on to smid_log[blockIdx.x]
+ * (used to check the SM budget; entries of CTAs not launched are left
+ * alone). */
 int tw_fused_reduce_add_rmsnorm_ex(const void* const* partials, int n_parts,
                                    const void* residual, const void* weight,
                                    void* const* out, int n_out,

@@ -95,8 +95,9 @@ typedef enum {
 
 /* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
 typedef enum {
-    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 8 tokens (when
-                          the row fits a cluster), rows kernel otherwise */
+    TW_PATH_AUTO = 0,  /* cluster kernel when every cluster of the range (one
+                          per token) can run at once on the device and the
+                          row fits a cluster, rows kernel otherwise */
     TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
                           staged into shared memory by bulk async copies */
     TW_PATH_WARP = 2,  /* one warp per token, no shared memory */

@@ -235,6 +235,24 @@ int cluster_set_attributes(int smem_optin) {
     return 0;
 }
 
+int cluster_max_active(int cluster, int* n) {
+    // Every instantiation asks for the same resources (128 threads, the
+    // exclusive-SM shared memory), so one stands for all.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = kExclusiveSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return static_cast<int>(
+        cudaOccupancyMaxActiveClusters(n, cluster_kernel_for(TW_BF16, 1), &cfg));
+}
+
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
                    bool pdl, void* stream) {
     const int vpt = cluster_vectors_per_thread(p.row_bytes, cluster);

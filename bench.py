@@ -453,7 +453,7 @@ def sweep(args, sync_ranks):
             for b in (2, 4, 8, 16, 148, 10 ** 6)}
         del res
     dec = {}
-    for T in sorted(set(inputs.DECODE_TOKENS) | {12, 16, 24, 32, 48}):
+    for T in sorted(set(inputs.DECODE_TOKENS) | {12, 16, 24, 32, 48, 96, 128}):
         res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
         dec[str(T)] = {path: entry(res.wl, graph_latency(res.launchers(path=path)))
                        for path in ("warp", "cluster", "rows", "auto")}

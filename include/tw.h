@@ -95,9 +95,10 @@ typedef enum {
 
 /* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
 typedef enum {
-    TW_PATH_AUTO = 0,  /* cluster kernel when every cluster of the range (one
-                          per token) can run at once on the device and the
-                          row fits a cluster, rows kernel otherwise */
+    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 64 tokens whose
+                          clusters (one per token) can all run at once on the
+                          device, when the row fits a cluster; rows kernel
+                          otherwise */
     TW_PATH_ROWS = 1,  /* persistent CTAs, one token per CTA at a time, rows
                           staged into shared memory by bulk async copies */
     TW_PATH_WARP = 2,  /* one warp per token, no shared memory */
@@ -105,7 +106,9 @@ typedef enum {
                            largest power of two <= min(8, max_sms)), the sum
                            of squares exchanged through distributed shared
                            memory; needs H * sizeof(dtype) <= C * 8 KB, else
-                           TW_ERR_UNSUPPORTED */
+                           TW_ERR_UNSUPPORTED.  Without a budget (max_sms at
+                           least the SM count) CTAs may share SMs when the
+                           clusters would not fit one CTA per SM. */
 } tw_path;
 
 /* The fused step on rows [t0, t1), bf16 tensors.  At most max_sms CTAs are

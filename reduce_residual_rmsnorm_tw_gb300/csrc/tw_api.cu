@@ -45,6 +45,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 // on this GPU (one warp cannot pull a 100+ KB token quickly) and runs only
 // when asked for.
 constexpr int64_t kClusterPathMaxTokens = 8;
+// AUTO never takes the cluster kernel beyond this many tokens (measured: at
+// 64 tokens it still beat the rows kernel, 4.1 vs 4.4 us; at 256 it lost,
+// 14.7 vs 9.5 us).
+constexpr int64_t kClusterAutoMaxTokens = 64;
 
 struct DeviceState {
     bool ready = false;
@@ -52,7 +56,9 @@ struct DeviceState {
     int smem_optin = 0;
     bool cluster_ready = false;
     const char* cluster_error = "";
-    int max_clusters[4] = {};  // clusters of 1, 2, 4, 8 CTAs that run at once
+    // Clusters of 1, 2, 4, 8 CTAs that run at once: [0] with every CTA alone
+    // on its SM (budgeted launches), [1] with CTAs free to share SMs.
+    int max_clusters[2][4] = {};
     unsigned int* status = nullptr;
     cudaEvent_t fork = nullptr;
     cudaEvent_t join = nullptr;
@@ -97,14 +103,17 @@ int device_state(DeviceState** out) {
             d.cluster_error = cudaGetErrorName(e);
             (void)cudaGetLastError();  // clear the (non-sticky) launch-API error
         }
-        for (int i = 0; d.cluster_ready && i < 4; ++i) {
-            int n = 0;
-            if (cluster_max_active(1 << i, &n) != cudaSuccess || n < 1) {
-                (void)cudaGetLastError();
-                n = static_cast<int>(kClusterPathMaxTokens);
+        for (int shared = 0; shared < 2; ++shared)
+            for (int i = 0; d.cluster_ready && i < 4; ++i) {
+                int n = 0;
+                if (cluster_max_active(1 << i, shared ? 0 : kExclusiveSmemBytes, &n) !=
+                        cudaSuccess ||
+                    n < 1) {
+                    (void)cudaGetLastError();
+                    n = static_cast<int>(kClusterPathMaxTokens);
+                }
+                d.max_clusters[shared][i] = n;
             }
-            d.max_clusters[i] = n;
-        }
         if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)) !=
             cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress");
@@ -269,12 +278,17 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
                         "the column-split mode and readiness flags run on the rows kernel only");
         path = TW_PATH_ROWS;
     }
+    int log2c = 0;
+    while ((2 << log2c) <= cluster) ++log2c;
+    // Clusters that run at once with every CTA alone on its SM, and (launches
+    // without a budget only) with CTAs sharing SMs.
+    const int64_t alone = d.cluster_ready ? d.max_clusters[0][log2c] : 0;
+    const int64_t shared = d.cluster_ready && pdl ? d.max_clusters[1][log2c] : 0;
     if (path == TW_PATH_AUTO) {
-        int log2c = 0;
-        while ((2 << log2c) <= cluster) ++log2c;
-        const int64_t at_once = d.cluster_ready ? d.max_clusters[log2c] : 0;
-        path = (tokens <= at_once && tokens * cluster <= sms && cluster_ok) ? TW_PATH_CLUSTER
-                                                                           : TW_PATH_ROWS;
+        const bool fits = pdl ? tokens <= (alone > shared ? alone : shared)
+                              : tokens <= alone && tokens * cluster <= sms;
+        path = (tokens <= kClusterAutoMaxTokens && fits && cluster_ok) ? TW_PATH_CLUSTER
+                                                                       : TW_PATH_ROWS;
     }
 
     int err;
@@ -296,9 +310,14 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
         if (!cluster_ok)
             return fail(TW_ERR_UNSUPPORTED, "row of %lld bytes too long for a cluster of %d",
                         (long long)p.row_bytes, cluster);
-        const int64_t max_clusters = sms / cluster;
+        // One CTA per SM (the exclusive shared-memory request) under a budget
+        // and whenever the clusters fit that way; otherwise, without a
+        // budget, CTAs share SMs so that more clusters run at once.
+        const bool share = pdl && tokens > alone && shared > sms / cluster;
+        int64_t max_clusters = share ? shared : sms / cluster;
         const int n_clusters = static_cast<int>(tokens < max_clusters ? tokens : max_clusters);
-        err = launch_cluster(p, a.dtype, cluster, n_clusters, kExclusiveSmemBytes, pdl, stream);
+        err = launch_cluster(p, a.dtype, cluster, n_clusters, share ? 0 : kExclusiveSmemBytes,
+                             pdl, stream);
     } else {
         return fail(TW_ERR_INVALID_ARG, "unknown path %d", path);
     }

@@ -235,13 +235,13 @@ int cluster_set_attributes(int smem_optin) {
     return 0;
 }
 
-int cluster_max_active(int cluster, int* n) {
-    // Every instantiation asks for the same resources (128 threads, the
-    // exclusive-SM shared memory), so one stands for all.
+int cluster_max_active(int cluster, size_t smem_bytes, int* n) {
+    // Every instantiation asks for the same resources (128 threads and the
+    // given dynamic shared memory), so one stands for all.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
     cfg.blockDim = dim3(kClusterThreads);
-    cfg.dynamicSmemBytes = kExclusiveSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);

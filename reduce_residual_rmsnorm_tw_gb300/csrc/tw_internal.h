@@ -88,9 +88,10 @@ int warp_set_smem_limit(int smem_optin);
 int cluster_set_attributes(int smem_optin);
 // Vectors per thread the cluster kernel needs (0: the row is too long).
 int cluster_vectors_per_thread(int64_t row_bytes, int cluster);
-// Clusters of `cluster` CTAs of the cluster kernel the current device can run
-// at once (cudaError_t as int).
-int cluster_max_active(int cluster, int* n);
+// Clusters of `cluster` CTAs of the cluster kernel, each CTA with smem_bytes of
+// dynamic shared memory, the current device can run at once (cudaError_t as
+// int).
+int cluster_max_active(int cluster, size_t smem_bytes, int* n);
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
                    bool pdl, void* stream);
 

@@ -55,8 +55,10 @@ def test_host_parity(wl, chunk):
 
 
 def test_host_matches_device_path_bitwise():
-    wl = CASES[0]
-    d, out, res_out = host_run(wl, 35)   # chunks of 35 tokens: the rows kernel
+    # Chunks of 100 tokens: above the automatic choice's cluster-kernel limit
+    # (64 tokens), so every chunk runs on the rows kernel.
+    wl = CASES[0].with_tokens(200)
+    d, out, res_out = host_run(wl, 100)
     dev_out = [torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")]
     dev_res = torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")
     tw.tw_fused_reduce_add_rmsnorm_ex([p.cuda() for p in d["partials"]], d["residual"].cuda(),

@@ -115,12 +115,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // 1-D bulk copy global -> this CTA's shared memory, completion counted on
 // `bar` as transaction bytes.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

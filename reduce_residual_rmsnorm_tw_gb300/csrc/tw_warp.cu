@@ -4,7 +4,9 @@
 // 融合内核): x = (sum_r partials[r]) + residual in fp32, ranks in order;
 // residual_out = x; out[k] = x / sqrt(mean x^2 + eps) * weight.
 //
-// A warp streams its token twice with 16-byte loads.  Pass 1 only accumulates
+// A warp streams its token twice with 16-byte loads, a step's loads for up to
+// eight partial rows and the residual issued before any is used.  Pass 1 only
+// accumulates
 // the sum of squares (loads keep the default L2 policy, so the row stays in
 // L2); the warp-shuffle total gives 1/rms.  Pass 2 recomputes x in the same
 // order -- bit-identical to pass 1 -- and stores residual_out and every gather
@@ -17,7 +19,8 @@ namespace tw {
 namespace {
 
 constexpr int kLaneVecs = 4;    // 16-byte vectors per lane per step
-constexpr int kPartGroup = 4;   // partial rows loaded together
+constexpr int kPartGroup = 8;   // partial rows loaded together (the residual
+                                // rides with the last group)
 
 // x for the kLaneVecs vectors idx0 + u*32 of token row `row_off` (bytes).
 // Vectors at or beyond nvec yield x = 0.
@@ -32,7 +35,11 @@ __device__ __forceinline__ void token_x(const Params& p, int64_t row_off, int64_
         for (int e = 0; e < E; ++e) x[u][e] = 0.f;
 
     for (int r0 = 0; r0 < p.n_parts; r0 += kPartGroup) {
+        // Every load of the group -- and, with the last group, the residual's
+        // -- is issued before any is used: one memory round trip per group.
+        const bool last = r0 + kPartGroup >= p.n_parts;
         uint4 raw[kPartGroup][kLaneVecs];
+        uint4 res[kLaneVecs];
 #pragma unroll
         for (int q = 0; q < kPartGroup; ++q)
 #pragma unroll
@@ -43,6 +50,13 @@ __device__ __forceinline__ void token_x(const Params& p, int64_t row_off, int64_
                                                row_off + idx * 16)
                                 : make_uint4(0, 0, 0, 0);
             }
+#pragma unroll
+        for (int u = 0; u < kLaneVecs; ++u) {
+            const int64_t idx = idx0 + u * 32;
+            res[u] = (last && idx < nvec)
+                         ? ld_global(static_cast<const char*>(p.residual) + row_off + idx * 16)
+                         : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int q = 0; q < kPartGroup; ++q) {
             if (r0 + q < p.n_parts) {
@@ -55,15 +69,15 @@ __device__ __forceinline__ void token_x(const Params& p, int64_t row_off, int64_
                 }
             }
         }
-    }
+        if (last) {
+            // The residual is added after every partial, as everywhere.
 #pragma unroll
-    for (int u = 0; u < kLaneVecs; ++u) {
-        const int64_t idx = idx0 + u * 32;
-        if (idx < nvec) {
-            float f[E];
-            V::to_float(ld_global(static_cast<const char*>(p.residual) + row_off + idx * 16), f);
+            for (int u = 0; u < kLaneVecs; ++u) {
+                float f[E];
+                V::to_float(res[u], f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) x[u][e] += f[e];
+                for (int e = 0; e < E; ++e) x[u][e] += f[e];
+            }
         }
     }
 }

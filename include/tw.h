@@ -216,8 +216,10 @@ int tw_split_launch(const void* const* partials, int n_parts,
  * staged in the workspace and copied back on a third stream, overlapping the
  * following chunks.  `stream` orders the whole call (it waits for the last
  * kernel or copy back).  The host buffers and the workspace are in use until
- * the work on `stream` completes.  Returns TW_ERR_INVALID_ARG if a tensor is
- * not page-locked host memory or the workspace is too small. */
+ * the work on `stream` completes.  A chunk_tokens above t1 - t0 is cut to
+ * t1 - t0 (the workspace is then checked against that chunk).  Returns
+ * TW_ERR_INVALID_ARG if a tensor is not page-locked host memory or the
+ * workspace is too small. */
 int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
                                      const void* residual, const void* weight,
                                      void* const* out, int n_out,
@@ -229,7 +231,9 @@ int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
                                      int dtype);
 
 /* Device workspace bytes tw_fused_reduce_add_rmsnorm_host needs: the weight
- * and two slots of (n_parts + 1 + n_out + 1) chunk buffers. */
+ * and two slots of (n_parts + 1 + n_out + 1) chunk buffers, each rounded up to
+ * 256 bytes.  TW_ERR_INVALID_ARG for arguments outside the rules above, or a
+ * chunk buffer (chunk_tokens * H * size) above 2^48 bytes. */
 int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H,
                             int64_t chunk_tokens, int dtype, size_t* bytes);
 
@@ -247,9 +251,12 @@ int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H,
  * TW_NOALLOC_SCRATCH_BYTES (16 MiB) that the library declares at file scope,
  * which every GPU that loads the library holds until the process exits.
  * Arguments are those of tw_fused_reduce_add_rmsnorm_host without the
- * workspace; chunk_tokens <= 0 picks the largest chunk that fits the array,
- * and a chunk whose staging needs more than the array holds is refused with
- * TW_ERR_UNSUPPORTED and a message naming both sizes.
+ * workspace, checked first (t0 == t1 then returns TW_OK with no CUDA call);
+ * chunk_tokens <= 0 picks the largest chunk, at most t1 - t0 tokens, whose
+ * staging fits the array; a larger chunk_tokens is cut to t1 - t0; a chunk
+ * whose staging needs more than the array holds is refused with
+ * TW_ERR_UNSUPPORTED and a message naming both sizes (every row fits: one
+ * token of the largest row and 25 buffers need under 2 MiB).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call on a device shares the one array and

@@ -351,6 +351,10 @@ int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
     if (rc != TW_OK) return rc;
     if (chunk_tokens < 1)
         return fail(TW_ERR_INVALID_ARG, "chunk_tokens %lld < 1", (long long)chunk_tokens);
+    // A chunk never needs to be longer than the range; capped so, its bytes
+    // stay within a buffer's (at most 2^48, checked above).
+    const int64_t span = a.t1 - a.t0 > 1 ? a.t1 - a.t0 : 1;
+    if (chunk_tokens > span) chunk_tokens = span;
     const int64_t rb = a.H * static_cast<int64_t>(elem_size(a.dtype));
     const size_t need = host_workspace_bytes(a.n_parts, a.n_out, rb, chunk_tokens);
     if (!workspace) return fail(TW_ERR_INVALID_ARG, "workspace is NULL");
@@ -400,6 +404,15 @@ int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
 }  // namespace
 
 int set_last_error(int code, const char* message) { return fail(code, "%s", message); }
+
+int check_host_args(const void* const* partials, int n_parts, const void* residual,
+                    const void* weight, void* const* out, int n_out, void* residual_out,
+                    int64_t T, int64_t H, float eps, int64_t t0, int64_t t1, int max_sms,
+                    int dtype) {
+    const Args a{partials, n_parts, residual, weight, out, n_out, residual_out,
+                 T,        H,       eps,      t0,     t1,  max_sms, dtype};
+    return check_args(a);
+}
 
 }  // namespace tw
 
@@ -521,10 +534,16 @@ int tw_split_launch(const void* const* partials, int n_parts, const void* residu
 int tw_host_workspace_bytes(int n_parts, int n_out, int64_t H, int64_t chunk_tokens, int dtype,
                             size_t* bytes) {
     if (!bytes || n_parts < 1 || n_parts > TW_MAX_PARTS || n_out < 1 || n_out > TW_MAX_OUTS ||
-        H < 1 || chunk_tokens < 1 || (dtype != TW_BF16 && dtype != TW_F32))
+        H < 1 || H > (dtype == TW_BF16 ? TW_MAX_H_BF16 : TW_MAX_H_F32) || chunk_tokens < 1 ||
+        (dtype != TW_BF16 && dtype != TW_F32))
         return tw::fail(TW_ERR_INVALID_ARG, "invalid workspace query");
-    *bytes = tw::host_workspace_bytes(n_parts, n_out, H * static_cast<int64_t>(tw::elem_size(dtype)),
-                                      chunk_tokens);
+    const int64_t rb = H * static_cast<int64_t>(tw::elem_size(dtype));
+    // A chunk buffer is at most 2^48 bytes (a device address range), so the
+    // size arithmetic below cannot overflow.
+    if (chunk_tokens > (int64_t{1} << 48) / rb)
+        return tw::fail(TW_ERR_INVALID_ARG, "chunks of %lld tokens of %lld bytes exceed 2^48 bytes",
+                        (long long)chunk_tokens, (long long)rb);
+    *bytes = tw::host_workspace_bytes(n_parts, n_out, rb, chunk_tokens);
     return TW_OK;
 }
 

@@ -13,11 +13,13 @@
 // until the process exits.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 #include <string>
 
 #include "tw.h"
+#include "tw_host.h"
 #include "tw_internal.h"
 
 namespace {
@@ -49,27 +51,47 @@ int scratch_for_current_device(void** out) {
     return 0;
 }
 
+// Staging bytes for chunks of k tokens, or SIZE_MAX if the query refuses k.
+size_t staging_bytes(int n_parts, int n_out, int64_t H, int dtype, int64_t k) {
+    size_t need = 0;
+    return tw_host_workspace_bytes(n_parts, n_out, H, k, dtype, &need) == TW_OK ? need : SIZE_MAX;
+}
+
+// The largest chunk in [1, span] whose staging fits the array, or 0 if not
+// even one token's does.  The staging size grows with the chunk (each chunk
+// buffer is rounded up to 256 bytes, so not by a fixed amount per token):
+// bisection over that monotone size, not an estimate of its slope.
+int64_t largest_fitting_chunk(int n_parts, int n_out, int64_t H, int dtype, int64_t span) {
+    if (staging_bytes(n_parts, n_out, H, dtype, 1) > kNoAllocScratchBytes) return 0;
+    int64_t lo = 1, hi = span;  // chunks of lo tokens fit
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo + 1) / 2;
+        if (staging_bytes(n_parts, n_out, H, dtype, mid) <= kNoAllocScratchBytes) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 }  // namespace
 
 extern "C" int tw_fused_reduce_add_rmsnorm_host_noalloc(
     const void* const* partials, int n_parts, const void* residual, const void* weight,
     void* const* out, int n_out, void* residual_out, int64_t T, int64_t H, float eps,
     int64_t t0, int64_t t1, int max_sms, int64_t chunk_tokens, void* stream, int dtype) {
-    // Pick the largest chunk that fits the array when none is given.
-    if (chunk_tokens <= 0) {
-        size_t one = 0;
-        int rc = tw_host_workspace_bytes(n_parts, n_out, H, 1, dtype, &one);
-        if (rc != TW_OK) return rc;
-        size_t two = 0;
-        rc = tw_host_workspace_bytes(n_parts, n_out, H, 2, dtype, &two);
-        if (rc != TW_OK) return rc;
-        const size_t per_token = two - one;  // bytes the workspace grows per chunk token
-        if (one > kNoAllocScratchBytes) chunk_tokens = 1;  // refused just below
-        else chunk_tokens = static_cast<int64_t>(1 + (kNoAllocScratchBytes - one) / per_token);
-    }
-    size_t need = 0;
-    int rc = tw_host_workspace_bytes(n_parts, n_out, H, chunk_tokens, dtype, &need);
+    int rc = tw::check_host_args(partials, n_parts, residual, weight, out, n_out, residual_out,
+                                 T, H, eps, t0, t1, max_sms, dtype);
     if (rc != TW_OK) return rc;
+    if (t0 == t1) return TW_OK;
+    // A chunk never needs to be longer than the range.
+    const int64_t span = t1 - t0;
+    if (chunk_tokens <= 0) {
+        // The largest chunk that fits the array.
+        chunk_tokens = largest_fitting_chunk(n_parts, n_out, H, dtype, span);
+        if (chunk_tokens == 0) chunk_tokens = 1;  // refused just below
+    } else if (chunk_tokens > span) {
+        chunk_tokens = span;
+    }
+    const size_t need = staging_bytes(n_parts, n_out, H, dtype, chunk_tokens);
     if (need > kNoAllocScratchBytes) {
         char buf[256];
         snprintf(buf, sizeof(buf),

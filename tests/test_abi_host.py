@@ -191,3 +191,97 @@ def test_flags_argument_checks(lib):
     assert f(*args, None, 1, 1) == INVALID                    # no flag array
     assert f(*args, BASE + 2, 1, 1) == ALIGN                  # misaligned flags
     assert f(*args, BASE + 128 * MB, 0, 1) == INVALID         # block_tokens 0
+
+
+GB = 1 << 30
+
+
+def noalloc(lib, H, dtype, n_parts, n_out, T, chunk_tokens, t0=0, t1=None):
+    """Call the no-allocation host entry point with fake, non-overlapping
+    addresses 1 GiB apart (every buffer here is smaller)."""
+    t1 = T if t1 is None else t1
+    p_arr = (ctypes.c_void_p * n_parts)(*[BASE + i * GB for i in range(n_parts)])
+    o_arr = (ctypes.c_void_p * n_out)(*[BASE + (20 + k) * GB for k in range(n_out)])
+    return lib.tw_fused_reduce_add_rmsnorm_host_noalloc(
+        p_arr, n_parts, BASE + 30 * GB, BASE + 31 * GB, o_arr, n_out, BASE + 32 * GB,
+        T, H, 1e-6, t0, t1, 8, chunk_tokens, None, dtype)
+
+
+# Rows of 8 to 16 KB, including rows whose staging size is not a whole number
+# of 256-byte units (H = 136, 152, 200 bf16), and rows of at most 128 bytes,
+# where one more token can leave the rounded staging size unchanged.
+NOALLOC_SHAPES = [(8, 0, 8, 2, 5000), (64, 0, 8, 2, 300), (136, 0, 8, 2, 7000),
+                  (152, 0, 1, 1, 20000), (200, 0, 8, 1, 1000), (8192, 0, 8, 2, 70),
+                  (4, 1, 4, 4, 100), (32, 1, 2, 1, 40000), (5120, 1, 4, 4, 8192)]
+
+
+@pytest.mark.parametrize("H,dtype,n_parts,n_out,T", NOALLOC_SHAPES)
+def test_noalloc_default_chunk_is_never_refused(lib, H, dtype, n_parts, n_out, T):
+    # chunk_tokens = 0 must size a chunk that fits the array: the call gets
+    # past the sizing to its first CUDA call (no device here: TW_ERR_CUDA; on
+    # a GPU machine the fake addresses are refused as not page-locked).
+    rc = noalloc(lib, H, dtype, n_parts, n_out, T, 0)
+    assert rc in (CUDA, INVALID), (rc, tw.tw_last_error_string())
+    assert "staging" not in tw.tw_last_error_string()
+
+
+@pytest.mark.parametrize("H,dtype,n_parts,n_out,T", NOALLOC_SHAPES)
+def test_noalloc_default_chunk_is_the_largest_that_fits(lib, H, dtype, n_parts, n_out, T):
+    # Closed form of the largest chunk: the workspace is the weight row plus
+    # 2 * (n_parts + n_out + 2) chunk buffers, each rounded up to 256 bytes,
+    # so k tokens fit 16 MiB iff k * row <= the per-buffer share rounded down
+    # to 256 bytes.
+    limit = 16 << 20
+    row = H * (2 if dtype == 0 else 4)
+    weight = -(-row // 256) * 256
+    share = (limit - weight) // (2 * (n_parts + n_out + 2)) // 256 * 256
+    k = min(T, share // row)
+    tdt = torch_bf16() if dtype == 0 else torch_f32()
+    assert tw.tw_host_workspace_bytes(n_parts, n_out, H, k, tdt) <= limit
+    if k < T:
+        assert tw.tw_host_workspace_bytes(n_parts, n_out, H, k + 1, tdt) > limit
+    # An explicit chunk of exactly k tokens is accepted, k + 1 refused.
+    assert noalloc(lib, H, dtype, n_parts, n_out, T, k) in (CUDA, INVALID)
+    assert "staging" not in tw.tw_last_error_string()
+    if k < T:
+        assert noalloc(lib, H, dtype, n_parts, n_out, T, k + 1) == UNSUP
+        assert "staging" in tw.tw_last_error_string()
+
+
+def test_noalloc_huge_and_oversized_chunks(lib):
+    # A chunk longer than the range is cut to the range: fits, no overflow.
+    assert noalloc(lib, 8192, 0, 8, 2, 4, 1 << 50) in (CUDA, INVALID)
+    assert noalloc(lib, 8192, 0, 8, 2, 4, (1 << 63) - 1) in (CUDA, INVALID)
+    assert "staging" not in tw.tw_last_error_string()
+    # 4096-token chunks of 16 KB rows need far more than 16 MiB.
+    assert noalloc(lib, 8192, 0, 8, 1, 8192, 4096) == UNSUP
+    # Argument rules come first; an empty range is a no-op with no CUDA call.
+    assert noalloc(lib, 8192, 0, 0, 1, 8, 0) == INVALID
+    assert noalloc(lib, 12, 0, 2, 1, 8, 0) == ALIGN
+    assert noalloc(lib, 8192, 0, 8, 1, 8, 0, t0=3, t1=3) == OK
+
+
+def test_workspace_query_refuses_overflowing_chunks(lib):
+    import ctypes as c
+    out = c.c_size_t()
+    assert lib.tw_host_workspace_bytes(8, 1, 8192, 1 << 50, 0, c.byref(out)) == INVALID
+    assert lib.tw_host_workspace_bytes(8, 1, 8192, (1 << 63) - 1, 0, c.byref(out)) == INVALID
+    assert lib.tw_host_workspace_bytes(8, 1, 8192, 1 << 20, 0, c.byref(out)) == OK
+    assert out.value == 2 * 11 * (1 << 20) * 16384 + 16384
+    # The host entry point cuts a huge chunk to its range before sizing the
+    # workspace (on a machine without a GPU the call then fails at its first
+    # CUDA call; with one, at the page-locked check of the fake addresses).
+    p_arr = (ctypes.c_void_p * 2)(BASE, BASE + GB)
+    o_arr = (ctypes.c_void_p * 1)(BASE + 20 * GB)
+    args = [p_arr, 2, BASE + 30 * GB, BASE + 31 * GB, o_arr, 1, BASE + 32 * GB, 4, 8192, 1e-6]
+    need4 = tw.tw_host_workspace_bytes(2, 1, 8192, 4, torch_bf16())
+    f = lib.tw_fused_reduce_add_rmsnorm_host
+    assert f(*args, 0, 4, 8, BASE + 40 * GB, need4, 1 << 50, None, 0) in (CUDA, INVALID)
+    assert "workspace" not in tw.tw_last_error_string()
+    assert f(*args, 0, 4, 8, BASE + 40 * GB, need4 - 256, 1 << 50, None, 0) == INVALID
+    assert "workspace" in tw.tw_last_error_string()
+
+
+def torch_f32():
+    import torch
+    return torch.float32

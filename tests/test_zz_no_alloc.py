@@ -65,3 +65,38 @@ def test_no_alloc_refuses_chunks_beyond_its_array():
     with pytest.raises(tw.TwError, match="TW_ERR_UNSUPPORTED"):
         tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
                                                     chunk_tokens=4096)
+
+
+# Default chunk (chunk_tokens = 0) on rows of 16 bytes to 20 KB, each range
+# long enough to need two or three chunks of the 16 MiB array: small rows
+# whose rounded staging grows by less than a row per token, and rows whose
+# staging is not a whole number of 256-byte units (H = 136 bf16).
+DEFAULT_CHUNK_CASES = [
+    Workload("noalloc_h8_bf16", 8, 50000, 8, "bf16", 1e-6, 2, 44),
+    Workload("noalloc_h64_bf16", 8, 6000, 64, "bf16", 1e-6, 2, 45),
+    Workload("noalloc_h136_bf16", 8, 3000, 136, "bf16", 1e-6, 2, 46),
+    Workload("noalloc_h8192_bf16", 8, 100, 8192, "bf16", 1e-5, 2, 47),
+    Workload("noalloc_h4_f32", 4, 60000, 4, "f32", 1e-6, 4, 48),
+    Workload("noalloc_h5120_f32", 4, 100, 5120, "f32", 1e-6, 4, 49),
+]
+
+
+@pytest.mark.parametrize("wl", DEFAULT_CHUNK_CASES, ids=lambda w: w.name)
+def test_no_alloc_default_chunk_matches_oracle(wl):
+    import oracle
+    parts, res, w = _pinned(wl)
+    out, res_out = _outputs(wl)
+    t0, t1 = 1, wl.T - 2
+    for _ in range(2):  # two calls in a row on the shared array
+        tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
+                                                    t0=t0, t1=t1)
+        torch.cuda.synchronize()
+        ref_out, ref_res = oracle.reordered([inputs.to_f64(p) for p in parts],
+                                            inputs.to_f64(res), inputs.to_f64(w), wl.eps,
+                                            n_out=wl.n_out, t0=t0, t1=t1)
+        for k in range(wl.n_out):
+            check_close(out[k][t0:t1], ref_out[k][t0:t1], wl.dtype, f"{wl.name} out[{k}]")
+            assert bool((torch.cat([out[k][:t0], out[k][t1:]]).float() == SENTINEL).all())
+        check_close(res_out[t0:t1], ref_res[t0:t1], wl.dtype, f"{wl.name} residual_out")
+        assert bool((torch.cat([res_out[:t0], res_out[t1:]]).float() == SENTINEL).all())
+    assert tw.tw_device_status() == 0

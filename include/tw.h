@@ -188,6 +188,19 @@ int tw_fused_reduce_add_rmsnorm_flags(const void* const* partials, int n_parts,
                                       const uint32_t* ready,
                                       int64_t block_tokens, uint32_t epoch);
 
+/* The producer side of the readiness flags (the FLUX notes' SetSignal):
+ * after all work queued earlier on `stream` has completed -- the kernels or
+ * copies that wrote the blocks' partial and residual rows -- set
+ * ready[first_block + i] = epoch for i in [0, n_blocks), each with a release
+ * store at GPU scope, so that tw_fused_reduce_add_rmsnorm_flags, whose
+ * acquire read sees the flag, also sees those rows.  A plain store or memset
+ * of the flags is a weak store and does not order the rows before the flag.
+ * `ready` is a DEVICE array of uint32, 4-byte aligned; first_block and
+ * n_blocks are in [0, 2^46]; n_blocks == 0 launches nothing.  Asynchronous
+ * on `stream` (one small kernel). */
+int tw_set_ready(uint32_t* ready, int64_t first_block, int64_t n_blocks,
+                 uint32_t epoch, void* stream);
+
 /* Two-chunk token split ("Der intelligente Split"): rows [0, t_split) run on
  * stream s0 and rows [t_split, T) on stream s1, each a rows-kernel launch with
  * its own budget of max_sms SMs (so up to 2*max_sms SMs while both run).

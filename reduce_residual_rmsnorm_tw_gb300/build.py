@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtw.so")
 SOURCES = ["tw_api.cu", "tw_rows.cu", "tw_warp.cu", "tw_cluster.cu", "tw_host.cu",
-           "tw_noalloc.cu"]
+           "tw_noalloc.cu", "tw_signal.cu"]
 HEADERS = ["tw_device.cuh", "tw_internal.h", "tw_host.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -60,6 +60,8 @@ def load():
     lib.tw_fused_reduce_add_rmsnorm_flags.argtypes = common + [
         ctypes.c_int, vp, i64, ctypes.c_uint32]
     lib.tw_fused_reduce_add_rmsnorm_flags.restype = ctypes.c_int
+    lib.tw_set_ready.argtypes = [vp, i64, i64, ctypes.c_uint32, vp]
+    lib.tw_set_ready.restype = ctypes.c_int
     lib.tw_split_launch.argtypes = [pp, ctypes.c_int, vp, vp, pp, ctypes.c_int,
                                     vp, i64, i64, ctypes.c_float, i64,
                                     ctypes.c_int, vp, vp, ctypes.c_int]
@@ -194,6 +196,20 @@ def tw_fused_reduce_add_rmsnorm_flags(partials, residual, weight, out,
         _ALL_SMS if max_sms is None else max_sms, _stream_handle(stream), dt,
         ready.data_ptr(), block_tokens, epoch & 0xFFFFFFFF)
     _check(rc)
+
+
+def tw_set_ready(ready, epoch, first_block=0, n_blocks=None, stream=None):
+    """Raise ``ready[first_block:first_block + n_blocks]`` (an int32 CUDA
+    tensor) to ``epoch`` with release stores, after the work queued earlier
+    on ``stream``: the producer side of tw_fused_reduce_add_rmsnorm_flags."""
+    if ready.dtype != torch.int32 or not ready.is_cuda or not ready.is_contiguous():
+        raise ValueError("ready must be a contiguous int32 CUDA tensor")
+    if n_blocks is None:
+        n_blocks = ready.numel() - first_block
+    if first_block < 0 or n_blocks < 0 or first_block + n_blocks > ready.numel():
+        raise ValueError("flag range outside the ready tensor")
+    _check(load().tw_set_ready(ready.data_ptr(), first_block, n_blocks, epoch & 0xFFFFFFFF,
+                               _stream_handle(stream)))
 
 
 def _typed(name, dtype):

@@ -113,3 +113,25 @@ def sample_tokens(T, n, seed, must=()):
     picks = set(rng.choice(T, size=min(n, T), replace=False).tolist())
     picks.update(t for t in must if 0 <= t < T)
     return sorted(picks)
+
+
+def check_chunked(wl, d, out, res_out, t0=0, t1=None, chunk=1024):
+    """Element-wise parity of a full-size run on EVERY row of [t0, t1): the
+    inputs (drawn on the device) are copied to the host `chunk` tokens at a
+    time and the oracle computes each chunk, so host memory stays small.
+    Destinations must also be bit-identical to out[0]."""
+    t1 = wl.T if t1 is None else t1
+    w = inputs.to_f64(d["weight"])
+    for c0 in range(t0, t1, chunk):
+        c1 = min(c0 + chunk, t1)
+        parts = [inputs.to_f64(p[c0:c1]) for p in d["partials"]]
+        ref_out, ref_res = oracle.reordered(parts, inputs.to_f64(d["residual"][c0:c1]), w,
+                                            wl.eps, n_out=wl.n_out)
+        del parts
+        for k in range(wl.n_out):
+            check_close(out[k][c0:c1], ref_out[k], wl.dtype, f"{wl.name} out[{k}] rows {c0}-{c1}")
+            if k:
+                assert torch.equal(out[k][c0:c1], out[0][c0:c1]), \
+                    f"{wl.name}: out[{k}] differs from out[0] in rows {c0}-{c1}"
+        check_close(res_out[c0:c1], ref_res, wl.dtype, f"{wl.name} residual_out rows {c0}-{c1}")
+

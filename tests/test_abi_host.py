@@ -285,3 +285,12 @@ def test_workspace_query_refuses_overflowing_chunks(lib):
 def torch_f32():
     import torch
     return torch.float32
+
+
+def test_set_ready_argument_checks(lib):
+    f = lib.tw_set_ready
+    assert f(None, 0, 1, 1, None) == INVALID
+    assert f(BASE + 2, 0, 1, 1, None) == ALIGN
+    assert f(BASE, -1, 1, 1, None) == INVALID
+    assert f(BASE, 0, -1, 1, None) == INVALID
+    assert f(BASE, 0, 0, 1, None) == OK              # nothing to raise: no launch

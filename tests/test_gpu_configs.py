@@ -1,13 +1,16 @@
 """The five benchmark workloads at full size, in the launch configuration the
-benchmark times, against the oracle: element by element where the oracle
-finishes in seconds (the N=2 and N=8 x 1024-token cases and the decode sweep),
-on sampled tokens otherwise (the 16384-token split and the fp32 column-split
-case, whose inputs are drawn on the device)."""
+benchmark times, against the oracle element by element on every row: the
+N=2 and N=8 x 1024-token cases and the decode sweep from host-drawn inputs;
+the 16384-token split and the fp32 column-split case from device-drawn
+inputs, compared in chunks of 1024 tokens (the oracle recomputes each chunk
+from the device inputs copied to the host), plus sampled rows at the chunk
+and split boundaries as an extra check."""
 import pytest
 import torch
 
 from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
-from tests.parity import alloc_outputs, check_sampled, check_workload, sample_tokens
+from tests.parity import (alloc_outputs, check_chunked, check_sampled, check_workload,
+                          sample_tokens)
 
 pytestmark = pytest.mark.gpu
 W = inputs.WORKLOADS
@@ -32,8 +35,8 @@ def test_decode_sweep_full(T, path):
     check_workload(W["decode_tp8_h8192_bf16"].with_tokens(T), path=path)
 
 
-@pytest.mark.parametrize("max_sms", [8, 148])
-def test_split_t16384_sampled(max_sms):
+@pytest.mark.parametrize("max_sms", [2, 8, 148])
+def test_split_t16384_every_row(max_sms):
     wl = W["split_tp8_t16384_h8192_bf16"]
     d = inputs.make_inputs(wl, device="cuda")
     out, res_out = alloc_outputs(wl)
@@ -44,14 +47,13 @@ def test_split_t16384_sampled(max_sms):
     tw.tw_split_launch(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps,
                        t_split=-1, max_sms=max_sms, s0=s0, s1=s1)
     s0.synchronize()
-    toks = sample_tokens(wl.T, 96, seed=3, must=(0, 1, 8191, 8192, 8193, wl.T - 1))
+    check_chunked(wl, d, out, res_out)
+    toks = sample_tokens(wl.T, 32, seed=3, must=(0, 1, 8191, 8192, 8193, wl.T - 1))
     check_sampled(wl, d, out, res_out, toks)
-    assert bool(torch.isfinite(out[0].float()).all())
-    assert bool(torch.isfinite(res_out.float()).all())
 
 
 @pytest.mark.parametrize("colsplit", [False, True])
-def test_colsplit_t8192_h5120_f32_sampled(colsplit):
+def test_colsplit_t8192_h5120_f32_every_row(colsplit):
     wl = W["colsplit_tp4_t8192_h5120_f32_out4"]
     d = inputs.make_inputs(wl, device="cuda")
     out, res_out = alloc_outputs(wl)
@@ -59,8 +61,6 @@ def test_colsplit_t8192_h5120_f32_sampled(colsplit):
           else tw.tw_fused_reduce_add_rmsnorm)
     fn(d["partials"], d["residual"], d["weight"], out, res_out, wl.eps)
     torch.cuda.synchronize()
-    toks = sample_tokens(wl.T, 128, seed=4, must=(0, wl.T - 1))
+    check_chunked(wl, d, out, res_out)
+    toks = sample_tokens(wl.T, 32, seed=4, must=(0, 1023, 1024, wl.T - 1))
     check_sampled(wl, d, out, res_out, toks)
-    for k in range(1, wl.n_out):
-        assert torch.equal(out[k], out[0])
-    assert bool(torch.isfinite(out[0]).all()) and bool(torch.isfinite(res_out).all())

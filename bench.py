@@ -6,19 +6,30 @@ inputs already resident in HBM.  Prints ONE JSON line (rank 0):
 
   value     tokens/s over all ranks (device time, CUDA events, max over ranks)
   roofline  achieved algorithmic GB/s of the kernel vs the measured HBM copy
-            peak; algorithmic bytes per token = (N + 1 + n_out + 1) * H * 2
+            peak; algorithmic bytes per token = (N + 1 + n_out + 1) * H * 2;
+            also the launch right after a different kernel (no launch of the
+            fused kernel before it to overlap with)
   e2e       the same metric through the C ABI with pinned HOST buffers: every
             step copies its inputs host->device, runs the kernel and copies the
             outputs back, all inside the timed region
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
-  sm_budget the same kernel held to 8 SMs
+  configs   every benchmark workload: the SM-budget sweep (2/4/8/16/148 and
+            the whole GPU) of the headline and of the 16384-token two-stream
+            split, the N=2 workload, the decode sizes on every kernel, the fp32
+            column split (dense read and column-split mode), the split
+            workload as one launch, the unfused torch chain
+  overlap   the fused kernel on a few SMs beside a bf16 GEMM, and the
+            two-chunk layer step
+  flags     readiness flags raised before the launch, and a live producer
+  clocks    nvidia-smi samples across every GPU leg of the run
 
 L2 (129 MB) is defeated by rotating through several buffer sets whose total
 is above 3x the L2 size, so every step streams from HBM.
 
 --impl reference times the oracle (the only reference this path has) on the
-host cores instead.  --sweep adds the SM-budget sweep, the decode sweep, the
-two-stream split and the fp32 column-split workload as extra fields.
+host cores instead.  --sweep adds the oracle on one thread and on all cores;
+--overlap the full GEMM-overlap sweep; --no-extra keeps only the headline,
+e2e and CPU legs.
 """
 import argparse
 import hashlib
@@ -51,6 +62,8 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--overlap", action="store_true",
                     help="add the GEMM / fused-kernel overlap measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload, overlap and flag legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -134,7 +147,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -151,12 +164,25 @@ class ClockSampler:
         rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 7]
         if not rows:
             return None
-        sm = [float(r[0]) for r in rows]
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        power = [num(r[2]) for r in rows if num(r[2]) is not None]
+        if not sm:
+            return None
+        # Samples under load: power at least 1.5x the lowest sample (idle
+        # moments between legs are left out of the median).
+        loaded = [num(r[0]) for r in rows if num(r[0]) is not None and num(r[2]) is not None
+                  and power and num(r[2]) >= 1.5 * min(power)]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]),
-                "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows
-                                                         if r[2].strip() not in ("", "[N/A]")),
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_mhz_all_samples":
+                statistics.median(sm), "sm_max_mhz": num(rows[0][1]), "samples": len(rows),
+                "samples_under_load": len(loaded), "power_w_max": max(power) if power else None,
                 "reasons": reasons}
 
 
@@ -429,84 +455,173 @@ def reference_main(args):
     return 0
 
 
-# ----------------------------------------------------------------- sweep ---
-def sweep(args, sync_ranks):
-    """SM-budget sweep, decode sweep, fp32 column split, the two-stream split
-    and the same tokens as one launch, the unfused torch chain, and the oracle
-    on one host thread and on all cores."""
-    import torch
-    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
-    W = inputs.WORKLOADS
-    peak, _ = measured_peaks()
+# -------------------------------------------------------- workload legs ---
+def rate(wl, ms, peak, tokens=None, bytes_per_token=None):
+    """Time per launch, tokens/s and algorithmic GB/s (fraction of `peak`)."""
+    tokens = wl.T if tokens is None else tokens
+    bpt = wl.bytes_per_token() if bytes_per_token is None else bytes_per_token
+    gbs = bpt * tokens / (ms * 1e-3) / 1e9
+    return {"launch_us": round(ms * 1e3, 2), "tokens_per_s": round(tokens / (ms * 1e-3)),
+            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+
+def budget_steps(max_sms):
+    """Launches per budget point: about 20 ms of work at the small budgets."""
+    if max_sms is None or max_sms >= 16:
+        return 200
+    return 20
+
+
+def budget_sweep(res, peak, budgets):
+    """The same launches held to each SM budget (None: the whole GPU, whose
+    launches may overlap the previous one's drain)."""
     out = {}
+    for b in budgets:
+        ms = device_leg(res, budget_steps(b), 3, max_sms=b)["mean_launch_ms"]
+        out["all" if b is None else str(b)] = rate(res.wl, ms, peak)
+    return out
 
-    def entry(wl, ms):
-        gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
-        return {"launch_us": round(ms * 1e3, 2), "tokens_per_s": wl.T / (ms * 1e-3),
-                "gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4)}
 
-    steps = max(50, min(args.steps, 2000))
-    for name in (HEADLINE, "tp2_t2048_h4096_bf16"):
-        res = Resident(W[name])
-        out[f"sm_budget:{name}"] = {
-            str(b): entry(res.wl, device_leg(res, steps, 20, max_sms=b)["mean_launch_ms"])
-            for b in (2, 4, 8, 16, 148, 10 ** 6)}
-        del res
-    dec = {}
-    for T in sorted(set(inputs.DECODE_TOKENS) | {12, 16, 24, 32, 48, 96, 128}):
-        res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
-        dec[str(T)] = {path: entry(res.wl, graph_latency(res.launchers(path=path)))
-                       for path in ("warp", "cluster", "rows", "auto")}
-        del res
-    out["decode_tp8_h8192_bf16"] = dec
-    out["decode_note"] = ("per-launch time of 200 back-to-back launches replayed from one "
-                          "CUDA graph, rotating resident batches")
-    # fp32 column split, four destinations: the dense read of all N zero-padded
-    # partials, and the column-split mode that reads each rank's slice only
-    # (GB/s counted against the dense algorithmic bytes; the column-split
-    # algorithmic bytes per token are (1 + 1 + n_out + 1) * H * 4).
-    res = Resident(W["colsplit_tp4_t8192_h5120_f32_out4"])
-    cs = {}
-    for mode in ("auto", "colsplit"):
-        ms = device_leg(res, max(20, steps // 20), 5, path=mode)["mean_launch_ms"]
-        cs["dense" if mode == "auto" else "colsplit"] = entry(res.wl, ms)
+def after_foreign_leg(res, peak, steps=200, spin_cycles=40000, gemm_k=8192):
+    """The headline launch right after a DIFFERENT kernel, so that it cannot
+    overlap the drain of a previous launch of itself: the region of `steps`
+    pairs [foreign kernel, fused launch] minus the region of the foreign
+    kernels alone, per step.  Two foreign kernels: a one-thread spin that
+    touches no memory (the fused launch starts on an idle memory system),
+    and a bf16 GEMM that writes partial 0 of the batch the fused launch then
+    reads (the row-parallel linear layer before it).  Each region is timed
+    twice, alternating, and the smaller is kept."""
+    import torch
+    stream = torch.cuda.Stream()
+    launchers = res.launchers()
+    n = len(launchers)
+    h = stream.cuda_stream
     wl = res.wl
-    cs_bytes = (1 + 1 + wl.n_out + 1) * wl.H * wl.elem_bytes * wl.T
-    cs["colsplit"]["colsplit_gbs"] = round(cs_bytes / (cs["colsplit"]["launch_us"] * 1e-6) / 1e9, 1)
-    cs["colsplit"]["colsplit_frac_of_measured_hbm"] = round(cs["colsplit"]["colsplit_gbs"] / peak, 4)
-    out["colsplit_tp4_t8192_h5120_f32_out4"] = cs
-    del res
-    # Two-chunk split on two streams (fork/join inside the library).
-    wl = W["split_tp8_t16384_h8192_bf16"]
+    x = torch.randn(wl.T, gemm_k, device="cuda", dtype=torch.bfloat16)
+    wmat = torch.randn(gemm_k, wl.H, device="cuda", dtype=torch.bfloat16) * (1.0 / gemm_k) ** 0.5
+    ranges = res.ranges()
+
+    def spin(i):
+        torch.cuda._sleep(spin_cycles)
+
+    def gemm(i):
+        t0, t1 = ranges[i % n]
+        torch.matmul(x, wmat, out=res.partials[0][t0:t1])
+
+    def region(foreign, with_fused):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                foreign(i)
+                if with_fused:
+                    launchers[i % n](h)
+            e0.record(stream)
+            for i in range(steps):
+                foreign(i)
+                if with_fused:
+                    launchers[i % n](h)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    out = {}
+    for name, foreign in (("spin", spin), ("gemm", gemm)):
+        both = min(region(foreign, True), region(foreign, True))
+        alone = min(region(foreign, False), region(foreign, False))
+        e = rate(wl, both - alone, peak)
+        e["foreign_us"] = round(alone * 1e3, 2)
+        out[name] = e
+    check_status()
+    del x, wmat
+    return out
+
+
+def decode_leg(W, peak, tokens=(1, 8, 12, 16, 24, 32, 48, 64, 96, 128, 256)):
+    """Decode-size ranges on every kernel: per-launch time of 200 launches
+    replayed from one CUDA graph."""
+    dec = {}
+    for T in tokens:
+        res = Resident(W["decode_tp8_h8192_bf16"].with_tokens(T))
+        dec[str(T)] = {path: round(graph_latency(res.launchers(path=path)) * 1e3, 2)
+                       for path in ("auto", "warp", "cluster", "rows")}
+        del res
+    return {"latency_us": dec,
+            "note": "per-launch time of 200 back-to-back launches replayed from one CUDA "
+                    "graph, rotating resident batches; auto is the library's choice"}
+
+
+def split_leg(wl, peak, budgets):
+    """tw_split_launch (the two-chunk split on two streams, default split
+    point) at each budget per chunk, and the same tokens as one launch."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import tw
     res = Resident(wl)
     s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     split = {}
-    for b in (2, 4, 8, 16, 148):
-        n_rep = 3 if b <= 4 else 20
+    for b in budgets:
+        n_rep = 3 if b is not None and b <= 4 else 10
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         for rep in range(n_rep + 1):
             if rep == 1:
                 evs[0].record(s0)
             t0, t1 = res.ranges()[rep % res.n_sets]
-            parts = [p[t0:t1] for p in res.partials]
-            tw.tw_split_launch(parts, res.residual[t0:t1], res.weight,
-                               [o[t0:t1] for o in res.out], res.residual_out[t0:t1],
+            tw.tw_split_launch([p[t0:t1] for p in res.partials], res.residual[t0:t1],
+                               res.weight, [o[t0:t1] for o in res.out], res.residual_out[t0:t1],
                                wl.eps, t_split=-1, max_sms=b, s0=s0, s1=s1)
         evs[1].record(s0)
         torch.cuda.synchronize()
-        split[str(b)] = entry(wl, evs[0].elapsed_time(evs[1]) / n_rep)
+        split["all" if b is None else str(b)] = rate(wl, evs[0].elapsed_time(evs[1]) / n_rep, peak)
     check_status()
-    out["split_tp8_t16384_h8192_bf16"] = split
-    # The same 16 384 tokens as one launch at the same budgets.
-    out["single_launch:split_tp8_t16384_h8192_bf16"] = {
-        str(b): entry(wl, device_leg(res, 3 if b <= 4 else 20, 2, max_sms=b)["mean_launch_ms"])
-        for b in (2, 4, 8, 16, 148)}
+    single = {}
+    for b in budgets:
+        steps = 3 if b is not None and b <= 4 else 10
+        ms = device_leg(res, steps, 2, max_sms=b)["mean_launch_ms"]
+        single["all" if b is None else str(b)] = rate(wl, ms, peak)
     del res
-    out["flags_raised:" + HEADLINE] = flags_leg(W[HEADLINE], steps)
-    out["unfused_torch_chain"] = unfused_leg(W[HEADLINE], steps)
-    out["oracle_threads"] = {str(n): cpu_baseline(W[HEADLINE], 5.0, threads=n)
-                             for n in (1, host_cores())}
+    return {"tw_split_launch": split, "one_launch": single,
+            "note": "budget per chunk for tw_split_launch (both chunks run at once: up to "
+                    "twice the budget while both run); budget per launch for one_launch"}
+
+
+def colsplit_leg(wl, peak):
+    """fp32 zero-padded column split, four destinations: the dense read of
+    all N partials, and the column-split mode that reads each rank's slice
+    only (its own algorithmic bytes per token: (1 + 1 + n_out + 1) * H * 4)."""
+    res = Resident(wl)
+    out = {}
+    for mode in ("auto", "colsplit"):
+        ms = device_leg(res, 20, 3, path=mode)["mean_launch_ms"]
+        out["dense" if mode == "auto" else "colsplit"] = rate(wl, ms, peak)
+    own = (1 + 1 + wl.n_out + 1) * wl.H * wl.elem_bytes
+    c = out["colsplit"]
+    c["own_bytes_per_token"] = own
+    c["own_gbs"] = round(own * wl.T / (c["launch_us"] * 1e-6) / 1e9, 1)
+    c["own_frac"] = round(c["own_gbs"] / peak, 4)
+    del res
+    return out
+
+
+def configs_leg(peak):
+    """Every benchmark workload: budgets, decode sizes, split, column split."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import inputs
+    W = inputs.WORKLOADS
+    budgets = list(inputs.SM_BUDGETS) + [None]
+    out = {}
+    for name in (HEADLINE, "tp2_t2048_h4096_bf16"):
+        res = Resident(W[name])
+        out[name] = {"sm_budget": budget_sweep(res, peak, budgets)}
+        del res
+        torch.cuda.empty_cache()
+    out["decode_tp8_h8192_bf16"] = decode_leg(W, peak)
+    out["split_tp8_t16384_h8192_bf16"] = split_leg(W["split_tp8_t16384_h8192_bf16"], peak, budgets)
+    torch.cuda.empty_cache()
+    out["colsplit_tp4_t8192_h5120_f32_out4"] = colsplit_leg(W["colsplit_tp4_t8192_h5120_f32_out4"],
+                                                            peak)
+    torch.cuda.empty_cache()
+    out["unfused_torch_chain"] = unfused_leg(W[HEADLINE], 200)
     return out
 
 
@@ -521,25 +636,79 @@ def flags_leg(wl, steps):
     peak, _ = measured_peaks()
     stream = torch.cuda.Stream()
     out = {}
-
-    def entry(ms):
-        gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
-        return {"launch_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-                "frac_of_measured_hbm": round(gbs / peak, 4)}
-
     region, _ = time_launches(res.launchers(), steps, 20, stream)
-    out["plain"] = entry(region / steps)
+    out["plain"] = rate(wl, region / steps, peak)
     for bt in (1, 64):
         ready = torch.ones(-(-res.big.T // bt), dtype=torch.int32, device="cuda")
         launchers = [tw.prepare(res.partials, res.residual, res.weight, res.out,
                                 res.residual_out, wl.eps, t0, t1, ready=ready,
                                 block_tokens=bt, epoch=1) for t0, t1 in res.ranges()]
         region, _ = time_launches(launchers, steps, 20, stream)
-        out[f"flags_block_{bt}"] = entry(region / steps)
+        out[f"raised_block_{bt}"] = rate(wl, region / steps, peak)
     check_status()
     del res
     torch.cuda.empty_cache()
+    out["live_producer"] = flags_live_leg(wl)
     return out
+
+
+def flags_live_leg(wl, block_tokens=64, budgets=(8, 32), gap_cycles=20000):
+    """A live producer: a second stream copies one block of 64 tokens' partial
+    and residual rows at a time into the buffers the consumer reads, raises
+    the block's flag with tw_set_ready and pauses (a spin of `gap_cycles`);
+    the consumer (tw_fused_reduce_add_rmsnorm_flags) was launched first, on a
+    budget that leaves SMs free for the producer.  Reports the producer's
+    span from its first copy to its last flag, the consumer's span from launch
+    to end, and how long the consumer ran after the last flag rose.  A
+    consumer wait that ran out (status word nonzero) is reported, and the
+    word cleared, rather than raised."""
+    import torch
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    src = inputs.make_inputs(wl, device="cuda")
+    src_t = src["partials"] + [src["residual"]]
+    dst = [torch.empty_like(t) for t in src_t]
+    out_t = [torch.empty_like(src["residual"]) for _ in range(wl.n_out)]
+    res_out = torch.empty_like(src["residual"])
+    n_blocks = -(-wl.T // block_tokens)
+    ready = torch.zeros(n_blocks, dtype=torch.int32, device="cuda")
+    consumer, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    result = {}
+    epoch = 0
+    for b_sms in budgets:
+        spans = []
+        for rep in range(3):
+            epoch += 1
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(consumer)
+            tw.tw_fused_reduce_add_rmsnorm_flags(dst[:-1], dst[-1], src["weight"], out_t, res_out,
+                                                 wl.eps, ready, block_tokens, epoch,
+                                                 max_sms=b_sms, stream=consumer)
+            ev[1].record(consumer)
+            with torch.cuda.stream(producer):
+                torch.cuda._sleep(100000)
+                ev[2].record(producer)
+                for b in range(n_blocks):
+                    rows = slice(b * block_tokens, min((b + 1) * block_tokens, wl.T))
+                    for d_t, s_t in zip(dst, src_t):
+                        d_t[rows].copy_(s_t[rows])
+                    tw.tw_set_ready(ready, epoch, first_block=b, n_blocks=1, stream=producer)
+                    if b + 1 < n_blocks:
+                        torch.cuda._sleep(gap_cycles)
+                ev[3].record(producer)
+            torch.cuda.synchronize()
+            spans.append((ev[2].elapsed_time(ev[3]), ev[0].elapsed_time(ev[1]),
+                          ev[3].elapsed_time(ev[1])))
+        status = tw.tw_device_status(clear=True)
+        prod, cons, tail = min(spans, key=lambda x: x[1])
+        result[str(b_sms)] = {
+            "producer_ms": round(prod, 4), "consumer_ms": round(cons, 4),
+            "consumer_after_last_flag_us": round(tail * 1e3, 1), "device_status": status}
+    result["note"] = (f"{n_blocks} blocks of {block_tokens} tokens; budget per consumer "
+                      f"launch; producer pauses {gap_cycles} cycles between blocks")
+    del src, dst, out_t, res_out
+    torch.cuda.empty_cache()
+    return result
 
 
 def unfused_leg(wl, steps):
@@ -571,26 +740,24 @@ def unfused_leg(wl, steps):
         e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
-    gbs = wl.bytes_per_token() * wl.T / (ms * 1e-3) / 1e9
     del res
     torch.cuda.empty_cache()
-    return {"workload": wl.name, "step_us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-            "frac_of_measured_hbm": round(gbs / peak, 4),
-            "chain": "torch.stack(partials).sum(0) + residual; rms_norm(x, weight, eps); "
-                     "copies into residual_out and out"}
+    e = rate(wl, ms, peak)
+    e["chain"] = ("torch.stack(partials).sum(0) + residual; rms_norm(x, weight, eps); "
+                  "copies into residual_out and out")
+    return e
 
 
 # --------------------------------------------------------------- overlap ---
-def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
+def overlap_leg(budgets=(8,), layer_budgets=(16, 48), gemm_reps=20):
     """The pages' overlap claim on one GPU ("Der intelligente Split", "Der
     Fused Kernel"): a compute-bound bf16 GEMM (torch.matmul, cuBLAS) on one
     stream while the fused kernel, held to a few SMs, runs on a second,
     higher-priority stream.  Reports the GEMM's slowdown and the fused
-    kernel's throughput alone and under overlap, and a two-chunk layer step
-    (GEMM(A); GEMM(B) beside fused(A); fused(B)) against the sequential order
-    (GEMM(A+B); fused(A+B)), the GEMM writing partial 0 of each chunk."""
+    kernel's throughput alone and under overlap, and the two-chunk layer
+    step (layer_step.two_chunk_layer_step) against the sequential order."""
     import torch
-    from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
+    from reduce_residual_rmsnorm_tw_gb300 import inputs, layer_step
     W = inputs.WORKLOADS
     peak, _ = measured_peaks()
     res = Resident(W[HEADLINE])
@@ -620,7 +787,6 @@ def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
     gemm_ms = e0.elapsed_time(e1) / gemm_reps
     out = {"gemm": {"shape": [M, N_, K], "ms": round(gemm_ms, 4),
                     "tflops": round(2 * M * N_ * K / (gemm_ms * 1e-3) / 1e12, 1)}}
-    bytes_launch = wl.bytes_per_token() * wl.T
     for bud in budgets:
         launchers = res.launchers(max_sms=bud)
         alone = device_leg(res, 10, 3, max_sms=bud)["mean_launch_ms"]
@@ -637,10 +803,9 @@ def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
         torch.cuda.synchronize()
         gemm_ov = g0.elapsed_time(g1) / gemm_reps
         fused_ov = f0.elapsed_time(f1) / n_fused
-        out[str(bud)] = {
-            "fused_alone_us": round(alone * 1e3, 1), "fused_overlap_us": round(fused_ov * 1e3, 1),
-            "fused_overlap_gbs": round(bytes_launch / (fused_ov * 1e-3) / 1e9, 1),
-            "gemm_overlap_ms": round(gemm_ov, 4), "gemm_slowdown": round(gemm_ov / gemm_ms, 4)}
+        out[f"fused_{bud}_sms_beside_gemm"] = {
+            "fused_alone": rate(wl, alone, peak), "fused_beside_gemm": rate(wl, fused_ov, peak),
+            "gemm_beside_fused_ms": round(gemm_ov, 4), "gemm_slowdown": round(gemm_ov / gemm_ms, 4)}
     check_status()
     del res, a, b, c
     torch.cuda.empty_cache()
@@ -653,30 +818,8 @@ def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
     ro = torch.empty_like(d["residual"])
     x = torch.randn(wl.T, 8192, device="cuda", dtype=torch.bfloat16)
     wmat = torch.randn(8192, wl.H, device="cuda", dtype=torch.bfloat16) * 0.01
-    half = wl.T // 2
     torch.cuda.synchronize()
-
-    def fused(t0, t1, budget, stream):
-        tw.tw_fused_reduce_add_rmsnorm(d["partials"], d["residual"], d["weight"], o, ro,
-                                       wl.eps, t0, t1, max_sms=budget, stream=stream)
-
-    def sequential():
-        with torch.cuda.stream(g):
-            torch.matmul(x, wmat, out=d["partials"][0])
-            fused(0, wl.T, None, g)
-
-    def two_chunk(budget):
-        done_a, done_b = torch.cuda.Event(), torch.cuda.Event()
-        with torch.cuda.stream(g):
-            torch.matmul(x[:half], wmat, out=d["partials"][0][:half])
-            done_a.record(g)
-            torch.matmul(x[half:], wmat, out=d["partials"][0][half:])
-            done_b.record(g)
-        f.wait_event(done_a)
-        fused(0, half, budget, f)
-        f.wait_event(done_b)
-        fused(half, wl.T, None, f)
-        g.wait_stream(f)
+    args = (x, wmat, d["partials"], d["residual"], d["weight"], o, ro, wl.eps)
 
     def timed(fn, reps=10):
         fn()
@@ -689,11 +832,14 @@ def overlap_leg(budgets=(2, 4, 8, 16, 32), gemm_reps=20):
         torch.cuda.synchronize()
         return s0.elapsed_time(s1) / reps
 
-    layer = {"sequential_ms": round(timed(sequential), 4)}
-    for bud in (8, 16, 32, 48, 64):
-        layer[f"two_chunk_budget_{bud}_ms"] = round(timed(lambda: two_chunk(bud)), 4)
+    layer = {"sequential_ms": round(timed(lambda: layer_step.sequential_layer_step(*args, g)), 4)}
+    for bud in layer_budgets:
+        layer[f"two_chunk_budget_{bud}_ms"] = round(
+            timed(lambda: layer_step.two_chunk_layer_step(*args, bud, g, f)), 4)
     check_status()
     out["layer_step_t16384"] = layer
+    del d, o, ro, x, wmat
+    torch.cuda.empty_cache()
     return out
 
 
@@ -738,22 +884,25 @@ def tw_main(args):
     wl = inputs.WORKLOADS[args.workload]
     if args.tokens is not None:
         wl = wl.with_tokens(args.tokens)
+    # Clocks are sampled from before the first launch to after the last GPU
+    # leg, so that even a short timed region is covered.
+    sampler = ClockSampler(device) if rank == 0 else None
     res = Resident(wl)
     l2_note = res.l2_note()
+    peak, peak_kind = measured_peaks()
 
-    sampler = ClockSampler(device) if rank == 0 else None
     dev = device_leg(res, args.steps, args.warmup, path=args.path, sync_ranks=sync_ranks)
-    clocks = sampler.stop() if sampler else None
-
     region_ms, launch_ms = max_over_ranks([dev["region_ms"], dev["mean_launch_ms"]], world)
     value = whole_job_tokens_per_s(world, wl.T, args.steps, region_ms)
-    peak, peak_kind = measured_peaks()
     algo_bytes = wl.bytes_per_token() * wl.T
     achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
 
-    diag = device_leg(res, min(args.steps, 2000), 20, path=args.path, per_launch=True)["events"]
-    sm8 = device_leg(res, max(50, min(args.steps, 2000)), 20, max_sms=8, path=args.path)
+    extra = not args.no_extra and rank == 0
+    diag = device_leg(res, max(20, min(args.steps, 2000)), 20, path=args.path,
+                      per_launch=True)["events"]
+    sm8 = device_leg(res, max(50, min(args.steps, 200)), 20, max_sms=8, path=args.path)
     sm8_gbs = algo_bytes / (sm8["mean_launch_ms"] * 1e-3) / 1e9
+    foreign = after_foreign_leg(res, peak) if extra else None
     del res
     torch.cuda.empty_cache()
 
@@ -772,13 +921,45 @@ def tw_main(args):
                        "chunked host->device copies overlapping the kernel on the previous "
                        "chunk, which stores its results straight into the mapped host "
                        "outputs (device->host copies where they are not mapped)"}
-    extra = sweep(args, None) if args.sweep and rank == 0 else None
-    overlap = overlap_leg() if args.overlap and rank == 0 else None
+    configs = configs_leg(peak) if extra else None
+    overlap = overlap_leg() if extra else None
+    if args.overlap and rank == 0:
+        overlap = overlap_leg(budgets=(2, 4, 8, 16, 32), layer_budgets=(8, 16, 32, 48, 64))
+    flags = flags_leg(inputs.WORKLOADS[HEADLINE], 200) if extra else None
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if clocks:
+        clocks["note"] = "nvidia-smi every 50 ms from before the first launch to after the last GPU leg"
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
+    threads = None
+    if args.sweep and rank == 0:
+        threads = {str(n): cpu_baseline(inputs.WORKLOADS[HEADLINE], 5.0, threads=n)
+                   for n in (1, host_cores())}
     if rank != 0:
         return 0
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": stored_traffic(wl.name), "peak_kind": peak_kind,
+                "frac_of_8tbs": round(achieved / 8000.0, 4),
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "mean_launch_us": round(launch_ms * 1e3, 2),
+                "launch_timing": "timed-region events over back-to-back launches "
+                                 "divided by the steps",
+                "events_per_launch_us": {
+                    "mean": round(diag["mean_launch_ms"] * 1e3, 2),
+                    "median": round(diag["median_launch_ms"] * 1e3, 2),
+                    "min": round(diag["min_launch_ms"] * 1e3, 2),
+                    "note": "diagnostic pass with an event pair around every launch "
+                            "(adds the launch gap, disables launch overlap)"}}
+    if foreign:
+        roofline["frac_after_foreign_kernel"] = foreign["spin"]["frac"]
+        roofline["after_foreign_kernel"] = foreign
+        roofline["after_foreign_kernel_note"] = (
+            "fused launch right after a different kernel: [foreign, fused] pairs minus the "
+            "foreign kernels alone; spin = a one-thread spin touching no memory, gemm = a bf16 "
+            "GEMM writing partial 0 of the batch the fused launch reads")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -789,28 +970,19 @@ def tw_main(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "sm_count": torch.cuda.get_device_properties(device).multi_processor_count},
         "hbm_gbs": round(achieved, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": stored_traffic(wl.name), "peak_kind": peak_kind,
-                     "frac_of_8tbs": round(achieved / 8000.0, 4),
-                     "algorithmic_bytes_per_launch": algo_bytes,
-                     "mean_launch_us": round(launch_ms * 1e3, 2),
-                     "launch_timing": "timed-region events over back-to-back launches "
-                                      "divided by the steps",
-                     "events_per_launch_us": {
-                         "mean": round(diag["mean_launch_ms"] * 1e3, 2),
-                         "median": round(diag["median_launch_ms"] * 1e3, 2),
-                         "min": round(diag["min_launch_ms"] * 1e3, 2),
-                         "note": "diagnostic pass with an event pair around every launch "
-                                 "(adds the launch gap, disables launch overlap)"}},
+        "roofline": roofline,
         "sm_budget_8": {"tokens_per_s": wl.T / (sm8["mean_launch_ms"] * 1e-3),
                         "gbs": round(sm8_gbs, 1), "frac": round(sm8_gbs / peak, 4)},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks,
     }
-    if extra is not None:
-        line["sweep"] = extra
+    if configs is not None:
+        line["configs"] = configs
     if overlap is not None:
         line["overlap"] = overlap
+    if flags is not None:
+        line["flags"] = flags
+    if threads is not None:
+        line["oracle_threads"] = threads
     print(json.dumps(line))
     return 0
 

@@ -672,6 +672,13 @@ def flags_live_leg(wl, block_tokens=64, budgets=(8, 32), gap_cycles=20000):
     n_blocks = -(-wl.T // block_tokens)
     ready = torch.zeros(n_blocks, dtype=torch.int32, device="cuda")
     consumer, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    # The producer's kernels run once before any consumer waits (a kernel's
+    # first launch may load it, and a load can wait for running kernels).
+    with torch.cuda.stream(producer):
+        torch.cuda._sleep(10)
+        dst[0][:1].copy_(src_t[0][:1])
+        tw.tw_set_ready(ready, 0, first_block=0, n_blocks=1, stream=producer)
+    torch.cuda.synchronize()
     result = {}
     epoch = 0
     for b_sms in budgets:

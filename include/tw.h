@@ -178,7 +178,13 @@ int tw_fused_reduce_add_rmsnorm_colsplit(const void* const* partials, int n_part
  * within about one second, the kernel stops reading and writing, sets the
  * value 4 in the device status word (tw_device_status) and returns; the rows
  * of the tokens that were waiting are then left unwritten (rows written before
- * are complete).  Runs on the rows kernel. */
+ * are complete).  Runs on the rows kernel.
+ * The producer's kernels must be loaded before this call starts waiting:
+ * under CUDA's lazy module loading (the default) a kernel is loaded at its
+ * first launch, and that load can wait for the kernels already running --
+ * this one, spinning on the flags -- so the waits run out (status 4).  Launch
+ * every producer kernel once beforehand; the library loads its own
+ * (tw_set_ready's) when it sets up a device. */
 int tw_fused_reduce_add_rmsnorm_flags(const void* const* partials, int n_parts,
                                       const void* residual, const void* weight,
                                       void* const* out, int n_out,

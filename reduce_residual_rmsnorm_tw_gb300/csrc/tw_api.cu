@@ -95,6 +95,11 @@ int device_state(DeviceState** out) {
         if ((e = static_cast<cudaError_t>(rows_set_smem_limit(d.smem_optin))) != cudaSuccess ||
             (e = static_cast<cudaError_t>(warp_set_smem_limit(d.smem_optin))) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute");
+        // Every kernel of the library is loaded here, before any of them can
+        // be waiting for another (lazy loading would load tw_set_ready's at
+        // its first launch, which may wait for running kernels).
+        if ((e = static_cast<cudaError_t>(signal_prepare())) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncGetAttributes");
         // The cluster kernel is optional: if it cannot be configured, that
         // path reports TW_ERR_UNSUPPORTED and the others still run.
         e = static_cast<cudaError_t>(cluster_set_attributes(d.smem_optin));

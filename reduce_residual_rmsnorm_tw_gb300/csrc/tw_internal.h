@@ -86,6 +86,9 @@ size_t rows_plan(Params& p, int smem_optin);
 int rows_set_smem_limit(int smem_optin);
 int warp_set_smem_limit(int smem_optin);
 int cluster_set_attributes(int smem_optin);
+// Load the readiness-flag producer kernel (tw_set_ready) on the current
+// device (cudaError_t as int).
+int signal_prepare();
 // Vectors per thread the cluster kernel needs (0: the row is too long).
 int cluster_vectors_per_thread(int64_t row_bytes, int cluster);
 // Clusters of `cluster` CTAs of the cluster kernel, each CTA with smem_bytes of

@@ -31,6 +31,15 @@ __global__ void __launch_bounds__(kSignalThreads)
 }
 
 }  // namespace
+
+int signal_prepare() {
+    // Loads the kernel now: with lazy module loading a kernel is loaded at its
+    // first launch, and that load may wait for kernels already running -- a
+    // consumer spinning on the very flags this kernel would raise.
+    cudaFuncAttributes attr;
+    return static_cast<int>(cudaFuncGetAttributes(&attr, set_ready_kernel));
+}
+
 }  // namespace tw
 
 extern "C" int tw_set_ready(uint32_t* ready, int64_t first_block, int64_t n_blocks,

@@ -93,6 +93,14 @@ def test_flags_live_producer(block_tokens):
     ready = torch.full((n_blocks,), epoch - 1, dtype=torch.int32, device="cuda")
     out, res_out = alloc_outputs(LIVE)
     consumer, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    # Every kernel the producer uses runs once before the consumer starts
+    # waiting: a kernel's first launch may load it, and a load can wait for
+    # the running consumer (lazy module loading).
+    with torch.cuda.stream(producer):
+        torch.cuda._sleep(10)
+        dst[0][:1].copy_(src[0][:1])
+        tw.tw_set_ready(ready, epoch - 1, first_block=0, n_blocks=1, stream=producer)
+    torch.cuda.synchronize()
     consumer.wait_stream(torch.cuda.current_stream())
     producer.wait_stream(torch.cuda.current_stream())
     ev = {k: torch.cuda.Event(enable_timing=True)

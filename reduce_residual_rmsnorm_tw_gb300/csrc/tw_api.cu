@@ -298,11 +298,13 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
 
     int err;
     if (path == TW_PATH_ROWS) {
+        p.unit_tokens = rows_unit_tokens(p, tokens, sms);
         const size_t smem = rows_plan(p, d.smem_optin);
         if (smem == 0)
             return fail(TW_ERR_UNSUPPORTED, "shared memory too small for rows of %lld bytes",
                         (long long)p.row_bytes);
-        const int grid = static_cast<int>(tokens < sms ? tokens : sms);
+        const int64_t units = (tokens + p.unit_tokens - 1) / p.unit_tokens;
+        const int grid = static_cast<int>(units < sms ? units : sms);
         err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
     } else if (path == TW_PATH_WARP) {
         const int64_t ctas = (tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta;

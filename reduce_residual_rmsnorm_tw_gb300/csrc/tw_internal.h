@@ -17,9 +17,15 @@ constexpr int kRowsMaxVecs = 4;
 // number of warps issuing copies, so a CTA that streams alone on its SM
 // issues from several.
 constexpr int kRowsMaxProducers = 2;
-// Target bytes of one ring stage of the rows kernel (whole input rows of one
-// token, at least one row).
+// Target bytes of one ring stage of the rows kernel (whole row groups of one
+// unit of tokens, at least one group).
 constexpr int kStageTargetBytes = 64 * 1024;
+// Tokens per unit of the rows kernel: at most kRowsMaxUnit consecutive tokens,
+// so that one bulk copy of a buffer's rows of the unit moves at most
+// kUnitCopyBytes (short rows move in larger copies; one issuing warp's copy
+// rate grows with the copy size).
+constexpr int kRowsMaxUnit = 4;
+constexpr int64_t kUnitCopyBytes = 16 * 1024;
 // Ring depth bounds of the rows kernel.
 constexpr int kMaxStages = 16;
 constexpr int kMinStages = 2;
@@ -55,7 +61,8 @@ struct Params {
     int64_t block_tokens;
     unsigned int epoch;
     int n_parts, n_out;
-    int rows_per_stage;     // rows kernel: whole input rows per ring stage
+    int unit_tokens;        // rows kernel: consecutive tokens per unit (1, 2 or 4)
+    int rows_per_stage;     // rows kernel: row groups (one buffer's rows of a unit) per stage
     int stages;             // rows kernel: ring depth (a multiple of producers)
     int producers;          // rows kernel: producer warps issuing copies (1..kRowsMaxProducers)
     int colsplit;           // 1: column-split mode
@@ -77,9 +84,13 @@ int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pd
                 void* stream);
 // Shared memory of the rows kernel for a stage size and ring depth.
 size_t rows_smem_bytes(size_t stage_bytes, int stages);
-// Launch plan of the rows kernel for p (row_bytes, n_parts and colsplit set):
-// sets rows_per_stage, stages and producers and returns the dynamic shared
-// memory to request, or 0 if the rows do not fit in smem_optin bytes.
+// Tokens per unit of the rows kernel for a range of `tokens` tokens on at
+// most `sms` CTAs (p's row_bytes, ready and colsplit set).
+int rows_unit_tokens(const Params& p, int64_t tokens, int64_t sms);
+// Launch plan of the rows kernel for p (row_bytes, n_parts, colsplit and
+// unit_tokens set): sets rows_per_stage, stages and producers and returns the
+// dynamic shared memory to request, or 0 if the rows do not fit in
+// smem_optin bytes.
 size_t rows_plan(Params& p, int smem_optin);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).

@@ -8,25 +8,28 @@
 //   out[k][t,h] = x * inv * weight[h]                 for every destination k
 //
 // Layout of the work: a token has R = N + 1 input rows (the N partials, then
-// the residual), each H * b contiguous bytes.  Producer warps stream them,
-// whole rows at a time, into a ring of shared-memory stages with 1-D bulk
-// async copies (cp.async.bulk, one copy per row, no tensor map, no
-// multicast); a stage holds `rows_per_stage` rows of one token (the host
-// picks a whole token when it fits, else an even split of its rows; a stage
-// never crosses into the next token) and is tracked by a "full" mbarrier
-// (transaction bytes) and an "empty" mbarrier (one arrival per consumer
-// warp).  The ring's stages are dealt round robin to `producers` warps (one
+// the residual), each H * b contiguous bytes.  CTAs take UNITS of U
+// consecutive tokens (U = 1, 2 or 4, fixed per launch), unit after unit with
+// a grid stride.  Producer warps stream a unit's rows into a ring of
+// shared-memory stages with 1-D bulk async copies (cp.async.bulk, no tensor
+// map, no multicast): one copy per input buffer and unit covers the U
+// consecutive rows of that buffer (contiguous in a row-major [T, H] tensor),
+// so short rows still move in large copies.  A stage holds `rows_per_stage`
+// such row groups of one unit (the host picks a whole unit when it fits, else
+// an even split of its groups; a stage never crosses into the next unit) and
+// is tracked by a "full" mbarrier (transaction bytes) and an "empty" mbarrier
+// (one arrival per consumer warp).  The ring's stages are dealt round robin to `producers` warps (one
 // elected lane each): the copy rate of one SM grows with the number of
 // warps issuing copies (one issuing warp streamed ~36 GB/s of 16 KB copies
 // whatever the ring depth, two ~69 GB/s), which is what bounds a CTA
 // streaming alone on its SM under a small SM budget.  Whole-row copies keep
 // several large copies from different buffers in flight.  The 512 consumer
-// threads own the 16-byte vectors tid, tid + 512, ... of the row: they add the
-// staged rows into fp32 registers in row order (ranks first, residual last),
-// store residual_out once the residual row is in, and after the token's last
-// stage the sum of squares goes through a warp shuffle and the 16 warp totals
-// through shared memory behind one named barrier; then the weighted result is
-// stored to every gather destination.  The N-way sum happens while the data
+// threads own the 16-byte vectors tid, tid + 512, ... of a row: for each
+// token of the unit they add the staged rows into fp32 registers in row
+// order (ranks first, residual last); after the unit's last stage each
+// token's sum of squares goes through a warp shuffle and the 16 warp totals
+// of every token of the unit through shared memory behind ONE named barrier;
+// then residual_out and the weighted result are stored for each token.  The N-way sum happens while the data
 // streams through shared memory, the counterpart of the pages' sum-at-load.
 //
 // Readiness flags (the FLUX notes' WaitSignal / SetSignal): with a `ready`
@@ -49,7 +52,7 @@ constexpr int kConsumerWarps = kRowsThreads / 32;
 constexpr int kFullOff = 0;
 constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
-constexpr int kAbortOff = kRedOff + 2 * kConsumerWarps * 4;
+constexpr int kAbortOff = kRedOff + 2 * kRowsMaxUnit * kConsumerWarps * 4;
 constexpr int kRingOff = 1024;
 // Tokens of its own a CTA prefetches into L2 before its first global read
 // (three measured best), never more than kPrefetchMaxBytes, so the prefetch
@@ -58,22 +61,25 @@ constexpr int kPrefetchTokens = 3;
 constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
 static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
 
-// Warm L2 with every input row of token t (bulk prefetches: nothing returns
-// to the SM and nothing waits on them).
-__device__ __forceinline__ void prefetch_token(const Params& p, int64_t t, int R, int n_sum) {
+// Warm L2 with every input row of the n_tok tokens from t (bulk prefetches:
+// nothing returns to the SM and nothing waits on them).
+__device__ __forceinline__ void prefetch_tokens(const Params& p, int64_t t, int n_tok, int R,
+                                                int n_sum) {
     const int64_t rb = p.row_bytes;
     const int64_t off = t * rb;
+    const uint32_t bytes = static_cast<uint32_t>(n_tok * rb);
     for (int g = 0; g < R; ++g) {
         if (g == n_sum) {
-            bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, static_cast<uint32_t>(rb));
+            bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, bytes);
         } else if (p.colsplit) {
-            for (int r = 0; r < p.n_parts; ++r)
-                if (p.col_lo[r] < p.col_lo[r + 1])
-                    bulk_prefetch_l2(static_cast<const char*>(p.partials[r]) + off + p.col_lo[r],
-                                     static_cast<uint32_t>(p.col_lo[r + 1] - p.col_lo[r]));
+            for (int j = 0; j < n_tok; ++j)
+                for (int r = 0; r < p.n_parts; ++r)
+                    if (p.col_lo[r] < p.col_lo[r + 1])
+                        bulk_prefetch_l2(static_cast<const char*>(p.partials[r]) + off + j * rb +
+                                             p.col_lo[r],
+                                         static_cast<uint32_t>(p.col_lo[r + 1] - p.col_lo[r]));
         } else {
-            bulk_prefetch_l2(static_cast<const char*>(p.partials[g]) + off,
-                             static_cast<uint32_t>(rb));
+            bulk_prefetch_l2(static_cast<const char*>(p.partials[g]) + off, bytes);
         }
     }
 }
@@ -96,11 +102,15 @@ struct RingPos {
 
 constexpr int kRowsBlock = kRowsThreads + 32 * kRowsMaxProducers;
 
-// FLAGS: the readiness-flag variant (p.ready set).  A separate instantiation,
-// so the plain kernel carries no flag code at all.
-template <typename T, int NV, bool FLAGS>
+// U: tokens per unit (1, 2 or 4); NV: 16-byte vectors per consumer thread
+// and row (U * NV <= kRowsMaxVecs registers' worth of x).  FLAGS: the
+// readiness-flag variant (p.ready set), only with U = 1.  Separate
+// instantiations, so the plain kernel carries no flag code at all.
+template <typename T, int NV, int U, bool FLAGS>
 __global__ void __launch_bounds__(kRowsBlock, 1)
     rows_kernel(const __grid_constant__ Params p) {
+    static_assert(U >= 1 && U <= kRowsMaxUnit && U * NV <= kRowsMaxVecs, "unit too large");
+    static_assert(!FLAGS || U == 1, "readiness flags take one token per unit");
     extern __shared__ __align__(1024) unsigned char smem[];
     using V = Vec<T>;
     constexpr int E = V::kElems;
@@ -110,11 +120,14 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     const int lane = tid & 31;
     const uint32_t S = static_cast<uint32_t>(p.stages);
     const int n_sum = p.colsplit ? 1 : p.n_parts;  // rows summed before the residual
-    const int R = n_sum + 1;                        // staged rows per token
-    const int G = p.rows_per_stage;
-    const int stages_per_token = (R + G - 1) / G;
+    const int R = n_sum + 1;                        // staged row groups per unit
+    const int G = p.rows_per_stage;                 // row groups per stage
+    const int stages_per_unit = (R + G - 1) / G;
     const int64_t rb = p.row_bytes;
-    const uint32_t stage_bytes = static_cast<uint32_t>(G * rb);
+    // A row group holds U consecutive token rows of one buffer (fewer in the
+    // range's last unit, which leaves the rest of its slot unused).
+    const uint32_t group_bytes = static_cast<uint32_t>(U * rb);
+    const uint32_t stage_bytes = static_cast<uint32_t>(G) * group_bytes;
     const uint32_t full0 = smem_addr(smem + kFullOff);
     const uint32_t empty0 = smem_addr(smem + kEmptyOff);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
@@ -131,6 +144,8 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         mbar_init_fence();
     }
     __syncthreads();
+    const int64_t first = p.t0 + static_cast<int64_t>(blockIdx.x) * U;  // first unit's token
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * U;
     // While the previous kernel of the stream drains (launches that may
     // overlap it only), warm L2 with this CTA's first tokens.  A prefetch only
     // fills L2, which is where every write of that kernel lands too, so data
@@ -139,15 +154,15 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     // are warmed (a raised flag means its rows are final); the first token
     // whose flag is not up ends the warming.
     if (warp == kConsumerWarps && lane == 0 && p.prefetch) {
-        const int64_t t_first = p.t0 + blockIdx.x;
-        const int64_t token_bytes = static_cast<int64_t>(R) * rb;
-        int64_t n_pre = kPrefetchTokens;
-        if (n_pre * token_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / token_bytes;
+        const int64_t unit_bytes = static_cast<int64_t>(R) * U * rb;
+        int64_t n_pre = (kPrefetchTokens + U - 1) / U;  // units
+        if (n_pre * unit_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / unit_bytes;
         for (int64_t i = 0; i < n_pre; ++i) {
-            const int64_t t = t_first + static_cast<int64_t>(i) * gridDim.x;
+            const int64_t t = first + i * stride;
             if (t >= p.t1) break;
             if (FLAGS && !flag_is_ready(p.ready + t / p.block_tokens, p.epoch)) break;
-            prefetch_token(p, t, R, n_sum);
+            const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+            prefetch_tokens(p, t, n_tok, R, n_sum);
         }
     }
     // Everything above touched only shared memory (and L2 through prefetches);
@@ -156,9 +171,6 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     grid_dependency_wait();
     grid_launch_dependents();
     if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
-
-    const int64_t first = p.t0 + blockIdx.x;
-    const int64_t stride = gridDim.x;
 
     if (warp >= kConsumerWarps) {
         // ----------------------------------------------------- producers ---
@@ -174,8 +186,10 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         bool stop = false;
         int64_t ready_block = -1;  // last flag block seen ready
         for (int64_t t = first; t < p.t1 && !stop; t += stride) {
+            const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+            const uint32_t copy_bytes = static_cast<uint32_t>(n_tok * rb);
             const int64_t row_off = t * rb;
-            for (int k = 0; k < stages_per_token; ++k, ++issued, pos.advance(S)) {
+            for (int k = 0; k < stages_per_unit; ++k, ++issued, pos.advance(S)) {
                 const uint32_t s = pos.stage;
                 if ((s & (P - 1)) != pw) continue;
                 if (FLAGS) {
@@ -199,24 +213,27 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                 const int g0 = k * G;
                 const int g1 = g0 + G < R ? g0 + G : R;
                 const uint32_t bar = full0 + 8 * s;
-                mbar_arrive_expect_tx(bar, static_cast<uint32_t>((g1 - g0) * rb));
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(g1 - g0) * copy_bytes);
                 uint32_t dst = ring_addr + s * stage_bytes;
-                for (int g = g0; g < g1; ++g, dst += static_cast<uint32_t>(rb)) {
+                for (int g = g0; g < g1; ++g, dst += group_bytes) {
                     if (g == n_sum) {
-                        bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off,
-                                 static_cast<uint32_t>(rb), bar, pol);
+                        bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off, copy_bytes,
+                                 bar, pol);
                     } else if (p.colsplit) {
-                        // One staged row from every rank's own column slice.
-                        for (int r = 0; r < p.n_parts; ++r) {
-                            const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
-                            if (lo < hi)
-                                bulk_g2s(dst + static_cast<uint32_t>(lo),
-                                         static_cast<const char*>(p.partials[r]) + row_off + lo,
-                                         static_cast<uint32_t>(hi - lo), bar, pol);
-                        }
+                        // One staged row per token from every rank's own
+                        // column slice.
+                        for (int j = 0; j < n_tok; ++j)
+                            for (int r = 0; r < p.n_parts; ++r) {
+                                const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
+                                if (lo < hi)
+                                    bulk_g2s(dst + static_cast<uint32_t>(j * rb + lo),
+                                             static_cast<const char*>(p.partials[r]) + row_off +
+                                                 j * rb + lo,
+                                             static_cast<uint32_t>(hi - lo), bar, pol);
+                            }
                     } else {
                         bulk_g2s(dst, static_cast<const char*>(p.partials[g]) + row_off,
-                                 static_cast<uint32_t>(rb), bar, pol);
+                                 copy_bytes, bar, pol);
                     }
                 }
             }
@@ -243,22 +260,25 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     const int64_t nvec = rb / 16;
     uint4 wv[NV];
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
-        wv[j] = v < nvec ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
-                         : make_uint4(0, 0, 0, 0);
+    for (int jj = 0; jj < NV; ++jj) {
+        const int64_t v = static_cast<int64_t>(jj) * kRowsThreads + tid;
+        wv[jj] = v < nvec ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
+                          : make_uint4(0, 0, 0, 0);
     }
 
     RingPos pos;
     int red_buf = 0;
     bool alive = true;
     for (int64_t t = first; t < p.t1; t += stride) {
-        float x[NV][E];
+        const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+        float x[U][NV][E];
 #pragma unroll
-        for (int j = 0; j < NV; ++j)
+        for (int j = 0; j < U; ++j)
 #pragma unroll
-            for (int e = 0; e < E; ++e) x[j][e] = 0.f;
-        for (int k = 0; k < stages_per_token; ++k, pos.advance(S)) {
+            for (int jj = 0; jj < NV; ++jj)
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[j][jj][e] = 0.f;
+        for (int k = 0; k < stages_per_unit; ++k, pos.advance(S)) {
             const uint32_t s = pos.stage;
             if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
                 give_up(p, abort_flag);
@@ -268,75 +288,118 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             const int g1 = g0 + G < R ? g0 + G : R;
             const unsigned char* stage = ring + s * stage_bytes + tid * 16;
             for (int g = g0; g < g1; ++g) {
-                const unsigned char* row = stage + (g - g0) * rb;
+                const unsigned char* group = stage + (g - g0) * group_bytes;
 #pragma unroll
-                for (int j = 0; j < NV; ++j)
-                    if (static_cast<int64_t>(j) * kRowsThreads + tid < nvec)
-                        add_vec(x[j],
-                                *reinterpret_cast<const uint4*>(row + j * kRowsThreads * 16),
-                                static_cast<T*>(nullptr));
+                for (int j = 0; j < U; ++j) {
+                    if (j < n_tok) {
+                        const unsigned char* row = group + j * rb;
+#pragma unroll
+                        for (int jj = 0; jj < NV; ++jj)
+                            if (static_cast<int64_t>(jj) * kRowsThreads + tid < nvec)
+                                add_vec(x[j][jj],
+                                        *reinterpret_cast<const uint4*>(row +
+                                                                        jj * kRowsThreads * 16),
+                                        static_cast<T*>(nullptr));
+                    }
+                }
             }
             __syncwarp();
             if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        // Every row is in, the residual last: store residual_out and reduce
-        // the sum of squares over the token.
-        float ss2[2] = {0.f, 0.f};
+        // Every row of the unit is in, the residual last: reduce each token's
+        // sum of squares (one barrier for the whole unit), then store.
+        float* red_unit = red + red_buf * (U * kConsumerWarps);
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
-            if (v < nvec) {
-                sum_squares<E>(ss2, x[j]);
-                if (alive)
-                    st_global_cs(static_cast<char*>(p.residual_out) + t * rb + v * 16,
-                                 V::from_float(x[j]));
-            }
+        for (int j = 0; j < U; ++j) {
+            float ss2[2] = {0.f, 0.f};
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj)
+                if (static_cast<int64_t>(jj) * kRowsThreads + tid < nvec)
+                    sum_squares<E>(ss2, x[j][jj]);
+            const float ss = warp_sum(ss2[0] + ss2[1]);
+            if (lane == 0) red_unit[j * kConsumerWarps + warp] = ss;
         }
-        const float ss = warp_sum(ss2[0] + ss2[1]);
-        if (lane == 0) red[red_buf * kConsumerWarps + warp] = ss;
         named_barrier(1, kRowsThreads);
-        float total = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) total += red[red_buf * kConsumerWarps + w];
         red_buf ^= 1;
-        const float inv = rsqrtf(total * p.inv_H + p.eps);
-
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int64_t v = static_cast<int64_t>(j) * kRowsThreads + tid;
-            if (v < nvec && alive) {
-                float w[E], y[E];
-                V::to_float(wv[j], w);
+        for (int j = 0; j < U; ++j) {
+            if (j >= n_tok) break;
+            float total = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) y[e] = (x[j][e] * inv) * w[e];
-                const uint4 packed = V::from_float(y);
-                for (int k = 0; k < p.n_out; ++k)
-                    st_global_cs(static_cast<char*>(p.out[k]) + t * rb + v * 16, packed);
+            for (int w = 0; w < kConsumerWarps; ++w) total += red_unit[j * kConsumerWarps + w];
+            const float inv = rsqrtf(total * p.inv_H + p.eps);
+            const int64_t row_off = (t + j) * rb;
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj) {
+                const int64_t v = static_cast<int64_t>(jj) * kRowsThreads + tid;
+                if (v < nvec && alive) {
+                    st_global_cs(static_cast<char*>(p.residual_out) + row_off + v * 16,
+                                 V::from_float(x[j][jj]));
+                    float w[E], y[E];
+                    V::to_float(wv[jj], w);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) y[e] = (x[j][jj][e] * inv) * w[e];
+                    const uint4 packed = V::from_float(y);
+                    for (int k = 0; k < p.n_out; ++k)
+                        st_global_cs(static_cast<char*>(p.out[k]) + row_off + v * 16, packed);
+                }
             }
         }
     }
 }
 
-template <typename T, bool FLAGS>
-void* rows_entry_for(int nv) {
-    switch (nv) {
-        case 1: return reinterpret_cast<void*>(&rows_kernel<T, 1, FLAGS>);
-        case 2: return reinterpret_cast<void*>(&rows_kernel<T, 2, FLAGS>);
-        case 3: return reinterpret_cast<void*>(&rows_kernel<T, 3, FLAGS>);
-        case 4: return reinterpret_cast<void*>(&rows_kernel<T, 4, FLAGS>);
+template <typename T, int NV, int U, bool FLAGS>
+void* rows_fn() {
+    return reinterpret_cast<void*>(&rows_kernel<T, NV, U, FLAGS>);
+}
+
+// The instantiation for a dtype, vectors per thread and unit size (nullptr
+// where U * nv is above kRowsMaxVecs or flags are asked with U > 1).
+template <typename T>
+void* rows_entry_for(int nv, int unit, bool flags) {
+    if (flags) {
+        if (unit != 1) return nullptr;
+        switch (nv) {
+            case 1: return rows_fn<T, 1, 1, true>();
+            case 2: return rows_fn<T, 2, 1, true>();
+            case 3: return rows_fn<T, 3, 1, true>();
+            case 4: return rows_fn<T, 4, 1, true>();
+            default: return nullptr;
+        }
+    }
+    switch (nv * 8 + unit) {
+        case 1 * 8 + 1: return rows_fn<T, 1, 1, false>();
+        case 1 * 8 + 2: return rows_fn<T, 1, 2, false>();
+        case 1 * 8 + 4: return rows_fn<T, 1, 4, false>();
+        case 2 * 8 + 1: return rows_fn<T, 2, 1, false>();
+        case 2 * 8 + 2: return rows_fn<T, 2, 2, false>();
+        case 3 * 8 + 1: return rows_fn<T, 3, 1, false>();
+        case 4 * 8 + 1: return rows_fn<T, 4, 1, false>();
         default: return nullptr;
     }
 }
 
-void* rows_kernel_for(int dtype, int nv, bool flags) {
-    if (dtype == TW_BF16)
-        return flags ? rows_entry_for<__nv_bfloat16, true>(nv)
-                     : rows_entry_for<__nv_bfloat16, false>(nv);
-    return flags ? rows_entry_for<float, true>(nv) : rows_entry_for<float, false>(nv);
+void* rows_kernel_for(int dtype, int nv, int unit, bool flags) {
+    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nv, unit, flags)
+                            : rows_entry_for<float>(nv, unit, flags);
 }
 
 int rows_vectors_per_thread(int64_t row_bytes) {
     return static_cast<int>((row_bytes / 16 + kRowsThreads - 1) / kRowsThreads);
+}
+
+// Tokens of the busiest CTA when `tokens` tokens are cut into units of u
+// (the last one ragged) dealt round robin to min(units, sms) CTAs.
+int64_t busiest_cta_tokens(int64_t tokens, int64_t u, int64_t sms) {
+    const int64_t units = (tokens + u - 1) / u;
+    const int64_t grid = units < sms ? units : sms;
+    const int64_t full = (units + grid - 1) / grid;  // units of the busiest CTAs
+    const int64_t r = units % grid;
+    const int64_t n_busiest = r == 0 ? grid : r;
+    if (n_busiest >= 2) return full * u;  // one of them holds whole units only
+    // The only busiest CTA (CTA 0) also holds the ragged last unit.
+    const int64_t last = tokens - (units - 1) * u;
+    return full * u - (u - last);
 }
 
 }  // namespace
@@ -345,17 +408,35 @@ size_t rows_smem_bytes(size_t stage_bytes, int stages) {
     return static_cast<size_t>(kRingOff) + static_cast<size_t>(stages) * stage_bytes;
 }
 
+int rows_unit_tokens(const Params& p, int64_t tokens, int64_t sms) {
+    // Units of several tokens only where one copy per row would be small and
+    // the unit does not lengthen the busiest CTA's share of the range: the
+    // largest U with U * row <= kUnitCopyBytes, U * vectors per thread within
+    // the register budget, and the busiest CTA's tokens no more than with
+    // one token per unit.  Readiness flags and the column-split mode take
+    // one token per unit.
+    if (p.ready || p.colsplit || tokens < 1 || sms < 1) return 1;
+    const int nv = rows_vectors_per_thread(p.row_bytes);
+    const int64_t share1 = busiest_cta_tokens(tokens, 1, sms);
+    for (int u = kRowsMaxUnit; u > 1; u /= 2) {
+        if (u * p.row_bytes > kUnitCopyBytes || u * nv > kRowsMaxVecs) continue;
+        if (busiest_cta_tokens(tokens, u, sms) <= share1) return u;
+    }
+    return 1;
+}
+
 size_t rows_plan(Params& p, int smem_optin) {
-    // Whole input rows of one token per stage: the whole token if its R rows
-    // fit kStageTargetBytes, else the token's rows split evenly over the
-    // fewest stages that fit (never more than R rows).  As many stages as fit
-    // the shared memory.
+    // Whole row groups of one unit per stage: the whole unit if its R groups
+    // fit kStageTargetBytes, else the unit's groups split evenly over the
+    // fewest stages that fit (never more than R groups).  As many stages as
+    // fit the shared memory.  p.unit_tokens must be set.
     const int64_t rows = p.colsplit ? 2 : p.n_parts + 1;
-    const int64_t parts = (rows * p.row_bytes + kStageTargetBytes - 1) / kStageTargetBytes;
+    const int64_t group = p.unit_tokens * p.row_bytes;
+    const int64_t parts = (rows * group + kStageTargetBytes - 1) / kStageTargetBytes;
     int64_t per_stage = (rows + parts - 1) / parts;
-    if (per_stage * p.row_bytes > kStageTargetBytes) per_stage = kStageTargetBytes / p.row_bytes;
+    if (per_stage * group > kStageTargetBytes) per_stage = kStageTargetBytes / group;
     if (per_stage < 1) per_stage = 1;
-    const size_t stage = static_cast<size_t>(per_stage * p.row_bytes);
+    const size_t stage = static_cast<size_t>(per_stage * group);
     int stages = static_cast<int>((static_cast<size_t>(smem_optin) - rows_smem_bytes(0, 0)) / stage);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < kMinStages) return 0;
@@ -377,18 +458,21 @@ size_t rows_plan(Params& p, int smem_optin) {
 int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
         for (int nv = 1; nv <= kRowsMaxVecs; ++nv)
-            for (bool flags : {false, true}) {
-                cudaError_t e = cudaFuncSetAttribute(rows_kernel_for(dt, nv, flags),
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     smem_optin);
-                if (e != cudaSuccess) return static_cast<int>(e);
-            }
+            for (int unit = 1; unit <= kRowsMaxUnit; unit *= 2)
+                for (bool flags : {false, true}) {
+                    void* fn = rows_kernel_for(dt, nv, unit, flags);
+                    if (!fn) continue;
+                    cudaError_t e = cudaFuncSetAttribute(
+                        fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+                    if (e != cudaSuccess) return static_cast<int>(e);
+                }
     return 0;
 }
 
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream) {
-    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.ready != nullptr);
+    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.unit_tokens,
+                               p.ready != nullptr);
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
     return launch_with_pdl(fn, p, grid, kRowsBlock, smem_bytes, pdl, stream);
 }

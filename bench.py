@@ -59,6 +59,8 @@ def parse_args():
                     help="override the workload's token count (e.g. decode sizes)")
     ap.add_argument("--path", default="auto", choices=["auto", "rows", "warp", "cluster"],
                     help="kernel of the timed leg")
+    ap.add_argument("--max-sms", type=int, default=None,
+                    help="SM budget of the timed leg (default: the whole GPU)")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--overlap", action="store_true",
                     help="add the GEMM / fused-kernel overlap measurement")
@@ -898,7 +900,8 @@ def tw_main(args):
     l2_note = res.l2_note()
     peak, peak_kind = measured_peaks()
 
-    dev = device_leg(res, args.steps, args.warmup, path=args.path, sync_ranks=sync_ranks)
+    dev = device_leg(res, args.steps, args.warmup, max_sms=args.max_sms, path=args.path,
+                     sync_ranks=sync_ranks)
     region_ms, launch_ms = max_over_ranks([dev["region_ms"], dev["mean_launch_ms"]], world)
     value = whole_job_tokens_per_s(world, wl.T, args.steps, region_ms)
     algo_bytes = wl.bytes_per_token() * wl.T
@@ -974,6 +977,7 @@ def tw_main(args):
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "n_parts": wl.n_parts, "T": wl.T, "H": wl.H,
                    "n_out": wl.n_out, "eps": wl.eps, "l2": l2_note, "path": args.path,
+                   "max_sms": args.max_sms or "all",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "sm_count": torch.cuda.get_device_properties(device).multi_processor_count},
         "hbm_gbs": round(achieved, 1),

@@ -57,14 +57,20 @@ def test_no_alloc_matches_workspace_entry_on_two_calls(dtype):
 
 
 def test_no_alloc_refuses_chunks_beyond_its_array():
-    wl = Workload("noalloc_big", 8, 4096, 8192, "bf16", 1e-5, 1, 43)
-    tiny = wl.with_tokens(4)
-    parts, res, w = _pinned(tiny)
-    out, res_out = _outputs(tiny)
-    # 4096-token chunks need 2 * 11 * 4096 * 16 KB of staging, far above 16 MiB.
+    wl = Workload("noalloc_big", 8, 64, 8192, "bf16", 1e-5, 1, 43)
+    parts, res, w = _pinned(wl)
+    out, res_out = _outputs(wl)
+    # 47-token chunks need 16 KB + 2 * 11 * 47 * 16 KB of staging, above 16 MiB
+    # (a chunk longer than the range would be cut to the range first).
     with pytest.raises(tw.TwError, match="TW_ERR_UNSUPPORTED"):
         tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
-                                                    chunk_tokens=4096)
+                                                    chunk_tokens=47)
+    # 46 tokens fit; nothing was written by the refused call.
+    assert bool((out[0].float() == SENTINEL).all())
+    tw.tw_fused_reduce_add_rmsnorm_host_noalloc(parts, res, w, out, res_out, wl.eps,
+                                                chunk_tokens=46)
+    torch.cuda.synchronize()
+    assert not bool((out[0].float() == SENTINEL).any())
 
 
 # Default chunk (chunk_tokens = 0) on rows of 16 bytes to 20 KB, each range

@@ -18,6 +18,9 @@ namespace {
 
 // Bounded-wait give-ups of any kernel on this device (see tw_device_status).
 __device__ unsigned int g_status_word;
+// Work counter pairs of the rows kernel (next unit, CTAs done); each launch
+// that claims units leaves its pair at zero when it ends.
+__device__ unsigned int g_work[2 * kWorkSlots];
 
 thread_local std::string t_last_error;
 
@@ -63,6 +66,15 @@ struct DeviceState {
     cudaEvent_t fork = nullptr;
     cudaEvent_t join = nullptr;
     std::mutex split_mu;  // orders the record/wait pairs of concurrent splits
+    // Work counter pairs: the device array, and per pair the event recorded
+    // after the last launch that used it (a pair is handed out again only
+    // once its event has completed).
+    unsigned int* work = nullptr;
+    cudaEvent_t work_done[kWorkSlots] = {};
+    bool work_used[kWorkSlots] = {};
+    bool work_bad[kWorkSlots] = {};
+    int work_next = 0;
+    std::mutex work_mu;
 };
 
 constexpr int kMaxDevices = 64;
@@ -125,6 +137,12 @@ int device_state(DeviceState** out) {
         if ((e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "cudaEventCreateWithFlags");
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.work), g_work)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress");
+        for (int k = 0; k < kWorkSlots; ++k)
+            if ((e = cudaEventCreateWithFlags(&d.work_done[k], cudaEventDisableTiming)) !=
+                cudaSuccess)
+                return cuda_fail(e, "cudaEventCreateWithFlags");
         d.ready = true;
     }
     *out = &d;
@@ -261,8 +279,36 @@ Params make_params(const Args& a, const DeviceState& d, int64_t t0, int64_t t1,
     return p;
 }
 
+// A work counter pair for a rows launch on `stream`, or -1 for a fixed
+// schedule: while the stream is being captured into a CUDA graph (a graph
+// replays the same pair, and no event can be polled), or when every pair is
+// still in use by a launch that has not completed.  Called with work_mu held.
+int acquire_work_slot(DeviceState& d, void* stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return -1;
+    for (int n = 0; n < kWorkSlots; ++n) {
+        const int k = (d.work_next + n) % kWorkSlots;
+        if (d.work_bad[k]) continue;
+        if (d.work_used[k]) {
+            const cudaError_t e = cudaEventQuery(d.work_done[k]);
+            if (e == cudaErrorNotReady) continue;
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                continue;
+            }
+        }
+        d.work_next = (k + 1) % kWorkSlots;
+        return k;
+    }
+    return -1;
+}
+
 // Launch one kernel over rows [t0, t1) (non-empty) on `stream`.
-int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, int path,
+int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path,
                  uint32_t* smid_log, void* stream) {
     const int64_t tokens = t1 - t0;
     const int64_t sms = a.max_sms < d.sm_count ? a.max_sms : d.sm_count;
@@ -305,7 +351,28 @@ int launch_range(const Args& a, const DeviceState& d, int64_t t0, int64_t t1, in
                         (long long)p.row_bytes);
         const int64_t units = (tokens + p.unit_tokens - 1) / p.unit_tokens;
         const int grid = static_cast<int>(units < sms ? units : sms);
-        err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
+        // Claimed units (a work counter pair of its own) whenever there are
+        // more units than CTAs (and fewer than 2^31, the counter's range);
+        // readiness flags keep the fixed schedule.
+        if (a.ready || units <= grid || units >= (int64_t{1} << 31)) {
+            err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
+        } else {
+            std::lock_guard<std::mutex> lock(d.work_mu);
+            const int slot = acquire_work_slot(d, stream);
+            p.work = slot >= 0 ? d.work + 2 * slot : nullptr;
+            err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
+            if (slot >= 0 && err == cudaSuccess) {
+                if (cudaEventRecord(d.work_done[slot], static_cast<cudaStream_t>(stream)) !=
+                    cudaSuccess) {
+                    // Without its event the pair could be handed out while
+                    // this launch runs: never use it again.
+                    (void)cudaGetLastError();
+                    d.work_bad[slot] = true;
+                } else {
+                    d.work_used[slot] = true;
+                }
+            }
+        }
     } else if (path == TW_PATH_WARP) {
         const int64_t ctas = (tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta;
         const int grid = static_cast<int>(ctas < sms ? ctas : sms);
@@ -387,7 +454,7 @@ int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
 
     const HostCall hc{a.partials, a.n_parts, a.residual, a.weight, a.out, a.n_out,
                       a.residual_out, rb, a.t0, a.t1, chunk_tokens, workspace, stream};
-    const DeviceState& dev = *d;
+    DeviceState& dev = *d;
     const LaunchChunk launch = [&](const void* const* parts, const void* residual,
                                    const void* weight, void* const* out, void* residual_out,
                                    int64_t n, cudaStream_t s) {

@@ -33,6 +33,10 @@ constexpr int kMinStages = 2;
 // an SM's 228 KB, so no two CTAs of a launch share an SM and a grid of at most
 // max_sms CTAs occupies at most max_sms SMs.
 constexpr int kExclusiveSmemBytes = 120 * 1024;
+// Work counters of the rows kernel per device: a launch that claims units
+// dynamically gets a pair of its own, handed out again only once that launch
+// has completed (an event per pair).
+constexpr int kWorkSlots = 64;
 // Warps per CTA of the warp-per-token kernel.
 constexpr int kWarpTokensPerCta = 4;
 // Cluster kernel: threads per CTA, largest cluster, vectors per thread bound.
@@ -48,6 +52,9 @@ struct Params {
     void* residual_out;
     uint32_t* smid_log;     // optional, rows kernel only
     unsigned int* status;   // device status word (bounded-wait give-ups)
+    // Rows kernel: this launch's work counter pair (next unit to claim, CTAs
+    // done claiming), zero at launch; NULL: a fixed unit schedule.
+    unsigned int* work;
     int64_t t0, t1;         // token range
     int64_t row_bytes;      // H * element size (multiple of 16)
     int64_t H;

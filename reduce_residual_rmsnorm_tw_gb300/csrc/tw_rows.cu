@@ -53,13 +53,23 @@ constexpr int kFullOff = 0;
 constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
 constexpr int kAbortOff = kRedOff + 2 * kRowsMaxUnit * kConsumerWarps * 4;
+// Claimed-unit bookkeeping: the unit index each stage carries, the queue of
+// claimed units producer 0 hands producer 1 ((unit, tag) pairs), and the last
+// queue position producer 1 has read.
+constexpr int kUnitQueue = 4;
+constexpr int kStageUnitOff = kAbortOff + 8;
+constexpr int kQueueOff = kStageUnitOff + 8 * kMaxStages;
+constexpr int kSeenOff = kQueueOff + 16 * kUnitQueue;
+// Two mbarriers that close a unit's sum-of-squares exchange among the
+// consumer warps (alternate units), so that every consumer wait is bounded.
+constexpr int kRedBarOff = kSeenOff + 8;
 constexpr int kRingOff = 1024;
 // Tokens of its own a CTA prefetches into L2 before its first global read
 // (three measured best), never more than kPrefetchMaxBytes, so the prefetch
 // of a whole grid stays well inside L2.
 constexpr int kPrefetchTokens = 3;
 constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
-static_assert(kAbortOff + 4 <= kRingOff, "shared header overflows");
+static_assert(kRedBarOff + 16 <= kRingOff, "shared header overflows");
 
 // Warm L2 with every input row of the n_tok tokens from t (bulk prefetches:
 // nothing returns to the SM and nothing waits on them).
@@ -106,6 +116,18 @@ constexpr int kRowsBlock = kRowsThreads + 32 * kRowsMaxProducers;
 // and row (U * NV <= kRowsMaxVecs registers' worth of x).  FLAGS: the
 // readiness-flag variant (p.ready set), only with U = 1.  Separate
 // instantiations, so the plain kernel carries no flag code at all.
+//
+// Unit schedule.  CTA b's first unit is unit b.  After that, with a work
+// counter (p.work), units are CLAIMED: producer 0 takes the next unit index
+// from the launch's counter (grid + an atomic increment) one unit ahead and
+// publishes it to producer 1 through a shared queue; the first stage of each
+// unit carries its index to the consumers, and a stage holding -1 (no unit
+// left) ends the consumers' loop.  SMs that stream faster therefore take
+// more units (on a GB300 some groups of SMs stream ~10 % slower than the
+// rest, and with a fixed share the whole launch waits for them).  Without a
+// counter (readiness flags, CUDA graph capture) CTA b takes units b,
+// b + grid, b + 2 grid, ...  Either way every unit is processed exactly once
+// and a token's arithmetic does not depend on which CTA processes it.
 template <typename T, int NV, int U, bool FLAGS>
 __global__ void __launch_bounds__(kRowsBlock, 1)
     rows_kernel(const __grid_constant__ Params p) {
@@ -130,36 +152,47 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     const uint32_t stage_bytes = static_cast<uint32_t>(G) * group_bytes;
     const uint32_t full0 = smem_addr(smem + kFullOff);
     const uint32_t empty0 = smem_addr(smem + kEmptyOff);
+    const uint32_t redbar0 = smem_addr(smem + kRedBarOff);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+    volatile int64_t* stage_unit = reinterpret_cast<volatile int64_t*>(smem + kStageUnitOff);
+    volatile int64_t* queue = reinterpret_cast<volatile int64_t*>(smem + kQueueOff);
+    volatile int64_t* p1_seen = reinterpret_cast<volatile int64_t*>(smem + kSeenOff);
     const unsigned char* ring = smem + kRingOff;
     const uint32_t ring_addr = smem_addr(ring);
+    const int64_t n_units = (p.t1 - p.t0 + U - 1) / U;
+    const bool claim = !FLAGS && p.work != nullptr;
 
     if (tid == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
+        mbar_init(redbar0, kConsumerWarps);
+        mbar_init(redbar0 + 8, kConsumerWarps);
         *abort_flag = 0;
+        for (int q = 0; q < kUnitQueue; ++q) queue[2 * q + 1] = -1;  // tags: nothing published
+        *p1_seen = 0;
         mbar_init_fence();
     }
     __syncthreads();
-    const int64_t first = p.t0 + static_cast<int64_t>(blockIdx.x) * U;  // first unit's token
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * U;
     // While the previous kernel of the stream drains (launches that may
-    // overlap it only), warm L2 with this CTA's first tokens.  A prefetch only
-    // fills L2, which is where every write of that kernel lands too, so data
-    // read after the wait below is current even if the previous kernel writes
-    // these rows.  With readiness flags only rows whose flag is already up
-    // are warmed (a raised flag means its rows are final); the first token
-    // whose flag is not up ends the warming.
+    // overlap it only), warm L2 with this CTA's first unit and the units a
+    // fixed schedule would give it next (with claimed units some other CTA
+    // takes those soon).  A prefetch only fills L2, which is where every
+    // write of that kernel lands too, so data read after the wait below is
+    // current even if the previous kernel writes these rows.  With readiness
+    // flags only rows whose flag is already up are warmed (a raised flag
+    // means its rows are final); the first token whose flag is not up ends
+    // the warming.
     if (warp == kConsumerWarps && lane == 0 && p.prefetch) {
         const int64_t unit_bytes = static_cast<int64_t>(R) * U * rb;
         int64_t n_pre = (kPrefetchTokens + U - 1) / U;  // units
         if (n_pre * unit_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / unit_bytes;
         for (int64_t i = 0; i < n_pre; ++i) {
-            const int64_t t = first + i * stride;
-            if (t >= p.t1) break;
+            const int64_t u = blockIdx.x + i * gridDim.x;
+            if (u >= n_units) break;
+            const int64_t t = p.t0 + u * U;
             if (FLAGS && !flag_is_ready(p.ready + t / p.block_tokens, p.epoch)) break;
             const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
             prefetch_tokens(p, t, n_tok, R, n_sum);
@@ -185,7 +218,72 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         uint64_t issued = 0;  // stages of the sequence passed, by any producer
         bool stop = false;
         int64_t ready_block = -1;  // last flag block seen ready
-        for (int64_t t = first; t < p.t1 && !stop; t += stride) {
+        // Claimed units: producer 0 publishes the unit of sequence position
+        // i in queue slot i % kUnitQueue as (unit, tag i); -1 = none left.
+        // It runs at most kUnitQueue - 1 positions ahead of producer 1's
+        // reads (p1_seen), so no slot is overwritten before it is read.
+        auto publish = [&](int64_t i, int64_t u) -> bool {
+            if (P > 1 && i - *p1_seen >= kUnitQueue) {
+                const uint64_t start = global_timer_ns();
+                while (i - *p1_seen >= kUnitQueue) {
+                    if (*abort_flag || global_timer_ns() - start > kWaitLimitNs) return false;
+                }
+            }
+            const int q = static_cast<int>(i % kUnitQueue);
+            queue[2 * q] = u;
+            __threadfence_block();
+            queue[2 * q + 1] = i;
+            return true;
+        };
+        int64_t u = blockIdx.x;  // every CTA has a first unit (grid <= units)
+        for (int64_t i = 0; !stop; ++i) {
+            if (i > 0) {
+                if (!claim) {
+                    u = blockIdx.x + i * gridDim.x;
+                    if (u >= n_units) break;
+                } else {
+                    // Unit of position i: producer 0 claimed it during
+                    // position i - 1; producer 1 waits (bounded) for it.
+                    const int q = static_cast<int>(i % kUnitQueue);
+                    if (pw != 0 && queue[2 * q + 1] != i) {
+                        const uint64_t start = global_timer_ns();
+                        while (queue[2 * q + 1] != i) {
+                            if (*abort_flag || global_timer_ns() - start > kWaitLimitNs) {
+                                give_up(p, abort_flag);
+                                stop = true;
+                                break;
+                            }
+                        }
+                        if (stop) break;
+                    }
+                    __threadfence_block();
+                    u = queue[2 * q];
+                    if (pw != 0) *p1_seen = i;
+                    if (u < 0) {
+                        // No unit left: the owner of the next stage hands the
+                        // consumers a stage holding -1 (an arrival without
+                        // bytes), which ends their loop.
+                        const uint32_t s = pos.stage;
+                        if ((s & (P - 1)) == pw) {
+                            if (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag)) {
+                                give_up(p, abort_flag);
+                            } else {
+                                stage_unit[s] = -1;
+                                mbar_arrive(full0 + 8 * s);
+                            }
+                        }
+                        ++issued;
+                        pos.advance(S);
+                        break;
+                    }
+                }
+            }
+            // Producer 0 claims the unit of position i + 1 now and publishes
+            // it once this unit's copies are issued, so the atomic's round
+            // trip overlaps them.
+            unsigned int claimed = 0;
+            if (claim && pw == 0) claimed = atomicAdd(p.work, 1u);
+            const int64_t t = p.t0 + u * U;
             const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
             const uint32_t copy_bytes = static_cast<uint32_t>(n_tok * rb);
             const int64_t row_off = t * rb;
@@ -210,6 +308,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                     stop = true;
                     break;
                 }
+                if (k == 0) stage_unit[s] = u;  // read by the consumers after the full wait
                 const int g0 = k * G;
                 const int g1 = g0 + G < R ? g0 + G : R;
                 const uint32_t bar = full0 + 8 * s;
@@ -236,6 +335,23 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                                  copy_bytes, bar, pol);
                     }
                 }
+            }
+            if (claim && pw == 0 && !stop) {
+                const int64_t next = static_cast<int64_t>(gridDim.x) + claimed;
+                if (!publish(i + 1, next < n_units ? next : -1)) {
+                    give_up(p, abort_flag);
+                    stop = true;
+                }
+            }
+        }
+        // The last CTA whose producer 0 is done claiming resets the counter
+        // for the launch that next gets it (the host hands a counter to a
+        // new launch only once the previous one has completed).
+        if (claim && pw == 0) {
+            __threadfence();
+            if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+                p.work[0] = 0;
+                p.work[1] = 0;
             }
         }
         // Drain: this producer's copies into its slots must have landed before
@@ -266,10 +382,31 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                           : make_uint4(0, 0, 0, 0);
     }
 
+    // Every consumer wait is bounded and its outcome is made uniform over the
+    // warp (__all_sync), and the warps meet per unit on an mbarrier, not a
+    // named barrier: a warp that gives up leaves the loop and the others
+    // give up at their next bounded wait instead of hanging.
+    constexpr unsigned kAll = 0xffffffffu;
     RingPos pos;
     int red_buf = 0;
-    bool alive = true;
-    for (int64_t t = first; t < p.t1; t += stride) {
+    uint32_t red_phase = 0;  // bit b: parity of the next phase of exchange barrier b
+    for (int64_t i = 0;; ++i) {
+        int64_t u = 0;
+        if (!claim) {
+            u = blockIdx.x + i * gridDim.x;
+            if (u >= n_units) break;
+        }
+        // The unit's first stage: with claimed units it carries the unit's
+        // index (-1: none left).
+        if (!__all_sync(kAll, mbar_wait(full0 + 8 * pos.stage, pos.phase, abort_flag))) {
+            give_up(p, abort_flag);
+            break;
+        }
+        if (claim) {
+            u = stage_unit[pos.stage];
+            if (u < 0) break;
+        }
+        const int64_t t = p.t0 + u * U;
         const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
         float x[U][NV][E];
 #pragma unroll
@@ -278,11 +415,12 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             for (int jj = 0; jj < NV; ++jj)
 #pragma unroll
                 for (int e = 0; e < E; ++e) x[j][jj][e] = 0.f;
+        bool ok = true;
         for (int k = 0; k < stages_per_unit; ++k, pos.advance(S)) {
             const uint32_t s = pos.stage;
-            if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
-                give_up(p, abort_flag);
-                alive = false;
+            if (k > 0 && !__all_sync(kAll, mbar_wait(full0 + 8 * s, pos.phase, abort_flag))) {
+                ok = false;
+                break;
             }
             const int g0 = k * G;
             const int g1 = g0 + G < R ? g0 + G : R;
@@ -304,10 +442,14 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                 }
             }
             __syncwarp();
-            if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        if (!ok) {
+            give_up(p, abort_flag);
+            break;
         }
         // Every row of the unit is in, the residual last: reduce each token's
-        // sum of squares (one barrier for the whole unit), then store.
+        // sum of squares (one exchange for the whole unit), then store.
         float* red_unit = red + red_buf * (U * kConsumerWarps);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
@@ -319,7 +461,17 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             const float ss = warp_sum(ss2[0] + ss2[1]);
             if (lane == 0) red_unit[j * kConsumerWarps + warp] = ss;
         }
-        named_barrier(1, kRowsThreads);
+        // Lane 0's arrival releases its totals; the wait acquires all 16.  A
+        // barrier's phase is reused two units later, after every warp has
+        // passed the other barrier, so no warp can run a phase ahead.
+        __syncwarp();
+        const uint32_t rbar = redbar0 + 8 * red_buf;
+        if (lane == 0) mbar_arrive(rbar);
+        if (!__all_sync(kAll, mbar_wait(rbar, (red_phase >> red_buf) & 1u, abort_flag))) {
+            give_up(p, abort_flag);
+            break;
+        }
+        red_phase ^= 1u << red_buf;
         red_buf ^= 1;
 #pragma unroll
         for (int j = 0; j < U; ++j) {
@@ -332,7 +484,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
 #pragma unroll
             for (int jj = 0; jj < NV; ++jj) {
                 const int64_t v = static_cast<int64_t>(jj) * kRowsThreads + tid;
-                if (v < nvec && alive) {
+                if (v < nvec) {
                     st_global_cs(static_cast<char*>(p.residual_out) + row_off + v * 16,
                                  V::from_float(x[j][jj]));
                     float w[E], y[E];

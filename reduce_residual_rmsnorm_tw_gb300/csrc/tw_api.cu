@@ -52,6 +52,12 @@ constexpr int64_t kClusterPathMaxTokens = 8;
 // 64 tokens it still beat the rows kernel, 4.1 vs 4.4 us; at 256 it lost,
 // 14.7 vs 9.5 us).
 constexpr int64_t kClusterAutoMaxTokens = 64;
+// Rows launches claim units from a work counter when they have at least this
+// many CTAs and units per CTA (on a GB300 this took the 8192- and 16384-token
+// workloads 5-10 % faster; launches of ~7 units per CTA or on a few SMs gained
+// nothing and lost to the counter's bookkeeping).
+constexpr int64_t kClaimMinGrid = 64;
+constexpr int64_t kClaimMinUnits = 16;
 
 struct DeviceState {
     bool ready = false;
@@ -351,10 +357,15 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
                         (long long)p.row_bytes);
         const int64_t units = (tokens + p.unit_tokens - 1) / p.unit_tokens;
         const int grid = static_cast<int>(units < sms ? units : sms);
-        // Claimed units (a work counter pair of its own) whenever there are
-        // more units than CTAs (and fewer than 2^31, the counter's range);
-        // readiness flags keep the fixed schedule.
-        if (a.ready || units <= grid || units >= (int64_t{1} << 31)) {
+        // Claimed units (a work counter pair of its own) for long launches on
+        // many SMs, where CTAs streaming at different speeds would otherwise
+        // finish far apart: at least kClaimMinGrid CTAs and kClaimMinUnits
+        // units per CTA (and fewer than 2^31 units, the counter's range).
+        // Shorter launches cannot rebalance by whole units and pay the
+        // counter's host-side bookkeeping; readiness flags keep the fixed
+        // schedule.
+        if (a.ready || grid < kClaimMinGrid || units < kClaimMinUnits * grid ||
+            units >= (int64_t{1} << 31)) {
             err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
         } else {
             std::lock_guard<std::mutex> lock(d.work_mu);

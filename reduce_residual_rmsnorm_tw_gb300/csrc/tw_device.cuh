@@ -148,6 +148,21 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also returns the OR of `pred` over the `threads`
+// participating threads (the same value in all of them).
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(any)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return any != 0;
+}
+
 // ---------------------------------------------------- 16-byte vectors ---
 // A 16-byte vector holds 8 bf16 or 4 fp32 elements.
 template <typename T>

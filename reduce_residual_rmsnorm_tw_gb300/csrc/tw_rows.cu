@@ -60,16 +60,13 @@ constexpr int kUnitQueue = 4;
 constexpr int kStageUnitOff = kAbortOff + 8;
 constexpr int kQueueOff = kStageUnitOff + 8 * kMaxStages;
 constexpr int kSeenOff = kQueueOff + 16 * kUnitQueue;
-// Two mbarriers that close a unit's sum-of-squares exchange among the
-// consumer warps (alternate units), so that every consumer wait is bounded.
-constexpr int kRedBarOff = kSeenOff + 8;
 constexpr int kRingOff = 1024;
 // Tokens of its own a CTA prefetches into L2 before its first global read
 // (three measured best), never more than kPrefetchMaxBytes, so the prefetch
 // of a whole grid stays well inside L2.
 constexpr int kPrefetchTokens = 3;
 constexpr int64_t kPrefetchMaxBytes = 720 * 1024;
-static_assert(kRedBarOff + 16 <= kRingOff, "shared header overflows");
+static_assert(kSeenOff + 8 <= kRingOff, "shared header overflows");
 
 // Warm L2 with every input row of the n_tok tokens from t (bulk prefetches:
 // nothing returns to the SM and nothing waits on them).
@@ -152,7 +149,6 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     const uint32_t stage_bytes = static_cast<uint32_t>(G) * group_bytes;
     const uint32_t full0 = smem_addr(smem + kFullOff);
     const uint32_t empty0 = smem_addr(smem + kEmptyOff);
-    const uint32_t redbar0 = smem_addr(smem + kRedBarOff);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
     volatile int64_t* stage_unit = reinterpret_cast<volatile int64_t*>(smem + kStageUnitOff);
@@ -168,8 +164,6 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
-        mbar_init(redbar0, kConsumerWarps);
-        mbar_init(redbar0 + 8, kConsumerWarps);
         *abort_flag = 0;
         for (int q = 0; q < kUnitQueue; ++q) queue[2 * q + 1] = -1;  // tags: nothing published
         *p1_seen = 0;
@@ -382,14 +376,13 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                           : make_uint4(0, 0, 0, 0);
     }
 
-    // Every consumer wait is bounded and its outcome is made uniform over the
-    // warp (__all_sync), and the warps meet per unit on an mbarrier, not a
-    // named barrier: a warp that gives up leaves the loop and the others
-    // give up at their next bounded wait instead of hanging.
-    constexpr unsigned kAll = 0xffffffffu;
+    // Every consumer wait is bounded.  The consumers meet once per unit at
+    // a named barrier that also ORs their "stop" votes (a wait that gave up,
+    // or no unit left), so they all leave the loop at the same barrier and
+    // none is left waiting there.
     RingPos pos;
     int red_buf = 0;
-    uint32_t red_phase = 0;  // bit b: parity of the next phase of exchange barrier b
+    bool alive = true;
     for (int64_t i = 0;; ++i) {
         int64_t u = 0;
         if (!claim) {
@@ -398,13 +391,15 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         }
         // The unit's first stage: with claimed units it carries the unit's
         // index (-1: none left).
-        if (!__all_sync(kAll, mbar_wait(full0 + 8 * pos.stage, pos.phase, abort_flag))) {
+        if (alive && !mbar_wait(full0 + 8 * pos.stage, pos.phase, abort_flag)) {
             give_up(p, abort_flag);
-            break;
+            alive = false;
         }
-        if (claim) {
+        bool none_left = false;
+        if (claim && alive) {
             u = stage_unit[pos.stage];
-            if (u < 0) break;
+            none_left = u < 0;
+            if (none_left) u = 0;
         }
         const int64_t t = p.t0 + u * U;
         const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
@@ -415,11 +410,11 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             for (int jj = 0; jj < NV; ++jj)
 #pragma unroll
                 for (int e = 0; e < E; ++e) x[j][jj][e] = 0.f;
-        bool ok = true;
-        for (int k = 0; k < stages_per_unit; ++k, pos.advance(S)) {
+        for (int k = 0; k < stages_per_unit && alive && !none_left; ++k, pos.advance(S)) {
             const uint32_t s = pos.stage;
-            if (k > 0 && !__all_sync(kAll, mbar_wait(full0 + 8 * s, pos.phase, abort_flag))) {
-                ok = false;
+            if (k > 0 && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
+                give_up(p, abort_flag);
+                alive = false;
                 break;
             }
             const int g0 = k * G;
@@ -444,12 +439,8 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        if (!ok) {
-            give_up(p, abort_flag);
-            break;
-        }
         // Every row of the unit is in, the residual last: reduce each token's
-        // sum of squares (one exchange for the whole unit), then store.
+        // sum of squares (one barrier for the whole unit), then store.
         float* red_unit = red + red_buf * (U * kConsumerWarps);
 #pragma unroll
         for (int j = 0; j < U; ++j) {
@@ -461,17 +452,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             const float ss = warp_sum(ss2[0] + ss2[1]);
             if (lane == 0) red_unit[j * kConsumerWarps + warp] = ss;
         }
-        // Lane 0's arrival releases its totals; the wait acquires all 16.  A
-        // barrier's phase is reused two units later, after every warp has
-        // passed the other barrier, so no warp can run a phase ahead.
-        __syncwarp();
-        const uint32_t rbar = redbar0 + 8 * red_buf;
-        if (lane == 0) mbar_arrive(rbar);
-        if (!__all_sync(kAll, mbar_wait(rbar, (red_phase >> red_buf) & 1u, abort_flag))) {
-            give_up(p, abort_flag);
-            break;
-        }
-        red_phase ^= 1u << red_buf;
+        if (named_barrier_or(1, kRowsThreads, !alive || none_left)) break;
         red_buf ^= 1;
 #pragma unroll
         for (int j = 0; j < U; ++j) {

@@ -1,7 +1,8 @@
-"""The rows kernel's unit schedule.  A launch with more units than CTAs lets
-its CTAs claim units from a work counter of its own (faster SMs take more);
-a launch captured into a CUDA graph keeps the fixed schedule (CTA b takes
-units b, b + grid, ...).  Either way every token is processed exactly once
+"""The rows kernel's unit schedule.  A long launch on many SMs (at least 64
+CTAs and 16 units per CTA) lets its CTAs claim units from a work counter of
+its own (faster SMs take more); other launches, and every launch captured
+into a CUDA graph, keep the fixed schedule (CTA b takes units b, b + grid,
+...).  Either way every token is processed exactly once
 and its result does not depend on which CTA processed it: both are checked
 bit for bit against each other and against the oracle, with many launches
 in flight at once on several streams (each needs a counter of its own) and
@@ -15,8 +16,12 @@ from tests.parity import alloc_outputs, check_workload
 
 pytestmark = pytest.mark.gpu
 
-WL = Workload("sched_tp8_t1500_h8192_bf16", 8, 1500, 8192, "bf16", 1e-5, 1, 81)
-SMALL = Workload("sched_tp3_t3001_h2048_bf16", 3, 3001, 2048, "bf16", 1e-6, 2, 82)
+# 3000 tokens of 16 KB rows: 19.7 units per CTA on 152 SMs, 30 on 100.
+WL = Workload("sched_tp2_t3000_h8192_bf16", 2, 3000, 8192, "bf16", 1e-5, 1, 81)
+# 13001 tokens of 4 KB rows: units of 2 tokens, 42.8 per CTA on 152 SMs.
+SMALL = Workload("sched_tp3_t13001_h2048_bf16", 3, 13001, 2048, "bf16", 1e-6, 2, 82)
+# 8 slices of 1100 tokens, each launched on 64 SMs (17.2 units per CTA).
+CONC = Workload("sched_tp2_t8800_h8192_bf16", 2, 8800, 8192, "bf16", 1e-6, 1, 83)
 
 
 def _launch(w, d, out, res_out, t0, t1, sms, stream):
@@ -24,8 +29,8 @@ def _launch(w, d, out, res_out, t0, t1, sms, stream):
                                       w.eps, t0, t1, max_sms=sms, path="rows", stream=stream)
 
 
-@pytest.mark.parametrize("w,sms", [(WL, None), (WL, 5), (SMALL, None), (SMALL, 3)],
-                         ids=["tp8_all", "tp8_sms5", "tp3_all", "tp3_sms3"])
+@pytest.mark.parametrize("w,sms", [(WL, None), (WL, 100), (WL, 5), (SMALL, None), (SMALL, 3)],
+                         ids=["tp2_all", "tp2_sms100", "tp2_sms5", "tp3_all", "tp3_sms3"])
 def test_claimed_units_equal_fixed_schedule_bitwise(w, sms):
     d = inputs.make_inputs(w, device="cuda")
     out_a, res_a = alloc_outputs(w)
@@ -44,17 +49,17 @@ def test_claimed_units_equal_fixed_schedule_bitwise(w, sms):
     assert tw.tw_device_status() == 0
 
 
-@pytest.mark.parametrize("w,sms", [(WL, None), (SMALL, 7)], ids=["tp8_all", "tp3_sms7"])
+@pytest.mark.parametrize("w,sms", [(WL, None), (SMALL, 64)], ids=["tp2_all", "tp3_sms64"])
 def test_claimed_units_match_oracle(w, sms):
     check_workload(w, path="rows", max_sms=sms)
     check_workload(w, path="rows", max_sms=sms, t0=17, t1=w.T - 5)
 
 
 def test_many_launches_in_flight_on_several_streams():
-    # 8 streams, each running 12 launches over its own slice of the range at a
-    # 3-SM budget: up to 8 launches run at once, 96 in all (more than the
-    # library's 64 counters, so counters are handed out again).
-    w = SMALL
+    # 8 streams, each running 12 launches over its own 1100-token slice on 64
+    # SMs: several launches run at once, each with its own counter, 96 in all
+    # (more than the library's 64 counters, so counters are handed out again).
+    w = CONC
     d = inputs.make_inputs(w, device="cuda")
     ref_out, ref_res = alloc_outputs(w)
     _launch(w, d, ref_out, ref_res, 0, w.T, None, None)
@@ -66,7 +71,7 @@ def test_many_launches_in_flight_on_several_streams():
         s.wait_stream(torch.cuda.current_stream())
     for rep in range(12):
         for i, s in enumerate(streams):
-            _launch(w, d, out, res_out, bounds[i], bounds[i + 1], 3, s)
+            _launch(w, d, out, res_out, bounds[i], bounds[i + 1], 64, s)
     torch.cuda.synchronize()
     for a, b in zip(out + [res_out], ref_out + [ref_res]):
         assert torch.equal(a, b)
@@ -85,7 +90,7 @@ def test_back_to_back_launches_reuse_counters():
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     for rep in range(200):
-        lo, hi = ((0, 900), (900, w.T))[rep % 2]
+        lo, hi = ((0, 2600), (2600, w.T))[rep % 2]
         _launch(w, d, out, res_out, lo, hi, None, s)
     torch.cuda.synchronize()
     for a, b in zip(out + [res_out], ref_out + [ref_res]):

@@ -109,27 +109,30 @@ struct RingPos {
 
 constexpr int kRowsBlock = kRowsThreads + 32 * kRowsMaxProducers;
 
-// U: tokens per unit (1, 2 or 4); NV: 16-byte vectors per consumer thread
-// and row (U * NV <= kRowsMaxVecs registers' worth of x).  FLAGS: the
-// readiness-flag variant (p.ready set), only with U = 1.  Separate
-// instantiations, so the plain kernel carries no flag code at all.
-//
-// Unit schedule.  CTA b's first unit is unit b.  After that, with a work
-// counter (p.work), units are CLAIMED: producer 0 takes the next unit index
-// from the launch's counter (grid + an atomic increment) one unit ahead and
-// publishes it to producer 1 through a shared queue; the first stage of each
-// unit carries its index to the consumers, and a stage holding -1 (no unit
-// left) ends the consumers' loop.  SMs that stream faster therefore take
-// more units (on a GB300 some groups of SMs stream ~10 % slower than the
-// rest, and with a fixed share the whole launch waits for them).  Without a
-// counter (readiness flags, CUDA graph capture) CTA b takes units b,
-// b + grid, b + 2 grid, ...  Either way every unit is processed exactly once
-// and a token's arithmetic does not depend on which CTA processes it.
-template <typename T, int NV, int U, bool FLAGS>
+// Kernel variants (separate instantiations, so each carries only its code):
+//   kFixed  -- CTA b takes units b, b + grid, b + 2 grid, ...
+//   kClaim  -- CTA b's first unit is b; after that producer 0 claims units
+//              from the launch's work counter (grid + an atomic increment),
+//              one unit ahead, and hands them to producer 1 through a shared
+//              queue; the first stage of each unit carries its index to the
+//              consumers, and a stage holding -1 (no unit left) ends their
+//              loop.  SMs that stream faster take more units (on a GB300
+//              some groups of SMs stream ~10 % slower than the rest; with a
+//              fixed share a long launch waits for them).
+//   kFlags  -- the fixed schedule, each token read only once its readiness
+//              flag is up.
+// Every unit is processed exactly once, and a token's arithmetic does not
+// depend on which CTA processes it.  U: tokens per unit (1, 2 or 4); NV:
+// 16-byte vectors per consumer thread and row (U * NV <= kRowsMaxVecs).
+constexpr int kFixed = 0, kClaim = 1, kFlags = 2;
+
+template <typename T, int NV, int U, int MODE>
 __global__ void __launch_bounds__(kRowsBlock, 1)
     rows_kernel(const __grid_constant__ Params p) {
     static_assert(U >= 1 && U <= kRowsMaxUnit && U * NV <= kRowsMaxVecs, "unit too large");
-    static_assert(!FLAGS || U == 1, "readiness flags take one token per unit");
+    static_assert(MODE != kFlags || U == 1, "readiness flags take one token per unit");
+    constexpr bool FLAGS = MODE == kFlags;
+    constexpr bool CLAIM = MODE == kClaim;
     extern __shared__ __align__(1024) unsigned char smem[];
     using V = Vec<T>;
     constexpr int E = V::kElems;
@@ -157,7 +160,6 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     const unsigned char* ring = smem + kRingOff;
     const uint32_t ring_addr = smem_addr(ring);
     const int64_t n_units = (p.t1 - p.t0 + U - 1) / U;
-    const bool claim = !FLAGS && p.work != nullptr;
 
     if (tid == 0) {
         for (uint32_t s = 0; s < S; ++s) {
@@ -165,20 +167,21 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         *abort_flag = 0;
-        for (int q = 0; q < kUnitQueue; ++q) queue[2 * q + 1] = -1;  // tags: nothing published
-        *p1_seen = 0;
+        if (CLAIM) {
+            for (int q = 0; q < kUnitQueue; ++q) queue[2 * q + 1] = -1;  // nothing published
+            *p1_seen = 0;
+        }
         mbar_init_fence();
     }
     __syncthreads();
     // While the previous kernel of the stream drains (launches that may
-    // overlap it only), warm L2 with this CTA's first unit and the units a
-    // fixed schedule would give it next (with claimed units some other CTA
-    // takes those soon).  A prefetch only fills L2, which is where every
-    // write of that kernel lands too, so data read after the wait below is
-    // current even if the previous kernel writes these rows.  With readiness
-    // flags only rows whose flag is already up are warmed (a raised flag
-    // means its rows are final); the first token whose flag is not up ends
-    // the warming.
+    // overlap it only), warm L2 with this CTA's first unit and the units the
+    // fixed schedule gives it next (with claimed units some other CTA takes
+    // those soon).  A prefetch only fills L2, which is where every write of
+    // that kernel lands too, so data read after the wait below is current
+    // even if the previous kernel writes these rows.  With readiness flags
+    // only rows whose flag is already up are warmed (a raised flag means its
+    // rows are final); the first token whose flag is not up ends the warming.
     if (warp == kConsumerWarps && lane == 0 && p.prefetch) {
         const int64_t unit_bytes = static_cast<int64_t>(R) * U * rb;
         int64_t n_pre = (kPrefetchTokens + U - 1) / U;  // units
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             if (u >= n_units) break;
             const int64_t t = p.t0 + u * U;
             if (FLAGS && !flag_is_ready(p.ready + t / p.block_tokens, p.epoch)) break;
-            const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+            const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
             prefetch_tokens(p, t, n_tok, R, n_sum);
         }
     }
@@ -212,32 +215,16 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         uint64_t issued = 0;  // stages of the sequence passed, by any producer
         bool stop = false;
         int64_t ready_block = -1;  // last flag block seen ready
-        // Claimed units: producer 0 publishes the unit of sequence position
-        // i in queue slot i % kUnitQueue as (unit, tag i); -1 = none left.
-        // It runs at most kUnitQueue - 1 positions ahead of producer 1's
-        // reads (p1_seen), so no slot is overwritten before it is read.
-        auto publish = [&](int64_t i, int64_t u) -> bool {
-            if (P > 1 && i - *p1_seen >= kUnitQueue) {
-                const uint64_t start = global_timer_ns();
-                while (i - *p1_seen >= kUnitQueue) {
-                    if (*abort_flag || global_timer_ns() - start > kWaitLimitNs) return false;
-                }
-            }
-            const int q = static_cast<int>(i % kUnitQueue);
-            queue[2 * q] = u;
-            __threadfence_block();
-            queue[2 * q + 1] = i;
-            return true;
-        };
-        int64_t u = blockIdx.x;  // every CTA has a first unit (grid <= units)
+        int64_t u = blockIdx.x;    // every CTA has a first unit (grid <= units)
         for (int64_t i = 0; !stop; ++i) {
             if (i > 0) {
-                if (!claim) {
+                if (!CLAIM) {
                     u = blockIdx.x + i * gridDim.x;
                     if (u >= n_units) break;
                 } else {
-                    // Unit of position i: producer 0 claimed it during
-                    // position i - 1; producer 1 waits (bounded) for it.
+                    // Unit of position i, claimed by producer 0 during
+                    // position i - 1 and published as (unit, tag i) in queue
+                    // slot i % kUnitQueue; producer 1 waits (bounded) for it.
                     const int q = static_cast<int>(i % kUnitQueue);
                     if (pw != 0 && queue[2 * q + 1] != i) {
                         const uint64_t start = global_timer_ns();
@@ -259,7 +246,8 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                         // bytes), which ends their loop.
                         const uint32_t s = pos.stage;
                         if ((s & (P - 1)) == pw) {
-                            if (issued >= S && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag)) {
+                            if (issued >= S &&
+                                !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag)) {
                                 give_up(p, abort_flag);
                             } else {
                                 stage_unit[s] = -1;
@@ -276,9 +264,9 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             // it once this unit's copies are issued, so the atomic's round
             // trip overlaps them.
             unsigned int claimed = 0;
-            if (claim && pw == 0) claimed = atomicAdd(p.work, 1u);
+            if (CLAIM && pw == 0) claimed = atomicAdd(p.work, 1u);
             const int64_t t = p.t0 + u * U;
-            const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+            const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
             const uint32_t copy_bytes = static_cast<uint32_t>(n_tok * rb);
             const int64_t row_off = t * rb;
             for (int k = 0; k < stages_per_unit; ++k, ++issued, pos.advance(S)) {
@@ -302,7 +290,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                     stop = true;
                     break;
                 }
-                if (k == 0) stage_unit[s] = u;  // read by the consumers after the full wait
+                if (CLAIM && k == 0) stage_unit[s] = u;  // read by the consumers after the full wait
                 const int g0 = k * G;
                 const int g1 = g0 + G < R ? g0 + G : R;
                 const uint32_t bar = full0 + 8 * s;
@@ -330,18 +318,34 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                     }
                 }
             }
-            if (claim && pw == 0 && !stop) {
+            if (CLAIM && pw == 0 && !stop) {
+                // Publish position i + 1, at most kUnitQueue - 1 positions
+                // ahead of producer 1's reads (p1_seen), so no queue slot is
+                // overwritten before it is read.
                 const int64_t next = static_cast<int64_t>(gridDim.x) + claimed;
-                if (!publish(i + 1, next < n_units ? next : -1)) {
-                    give_up(p, abort_flag);
-                    stop = true;
+                const int64_t j = i + 1;
+                if (P > 1 && j - *p1_seen >= kUnitQueue) {
+                    const uint64_t start = global_timer_ns();
+                    while (j - *p1_seen >= kUnitQueue) {
+                        if (*abort_flag || global_timer_ns() - start > kWaitLimitNs) {
+                            give_up(p, abort_flag);
+                            stop = true;
+                            break;
+                        }
+                    }
+                }
+                if (!stop) {
+                    const int q = static_cast<int>(j % kUnitQueue);
+                    queue[2 * q] = next < n_units ? next : -1;
+                    __threadfence_block();
+                    queue[2 * q + 1] = j;
                 }
             }
         }
         // The last CTA whose producer 0 is done claiming resets the counter
         // for the launch that next gets it (the host hands a counter to a
         // new launch only once the previous one has completed).
-        if (claim && pw == 0) {
+        if (CLAIM && pw == 0) {
             __threadfence();
             if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
                 p.work[0] = 0;
@@ -376,16 +380,18 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                           : make_uint4(0, 0, 0, 0);
     }
 
-    // Every consumer wait is bounded.  The consumers meet once per unit at
-    // a named barrier that also ORs their "stop" votes (a wait that gave up,
-    // or no unit left), so they all leave the loop at the same barrier and
-    // none is left waiting there.
+    // Every consumer wait is bounded and every consumer passes the unit's
+    // named barrier once per unit.  Fixed schedule: all consumers walk the
+    // same units, and one that gave up keeps walking them (no waits, no
+    // stores) so the barrier sequence stays whole.  Claimed units: the
+    // barrier ORs the consumers' "stop" votes (a wait that gave up, or no
+    // unit left), so all leave the loop at the same barrier.
     RingPos pos;
     int red_buf = 0;
     bool alive = true;
     for (int64_t i = 0;; ++i) {
         int64_t u = 0;
-        if (!claim) {
+        if (!CLAIM) {
             u = blockIdx.x + i * gridDim.x;
             if (u >= n_units) break;
         }
@@ -396,13 +402,13 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             alive = false;
         }
         bool none_left = false;
-        if (claim && alive) {
+        if (CLAIM && alive) {
             u = stage_unit[pos.stage];
             none_left = u < 0;
             if (none_left) u = 0;
         }
         const int64_t t = p.t0 + u * U;
-        const int n_tok = p.t1 - t < U ? static_cast<int>(p.t1 - t) : U;
+        const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
         float x[U][NV][E];
 #pragma unroll
         for (int j = 0; j < U; ++j)
@@ -410,12 +416,12 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             for (int jj = 0; jj < NV; ++jj)
 #pragma unroll
                 for (int e = 0; e < E; ++e) x[j][jj][e] = 0.f;
-        for (int k = 0; k < stages_per_unit && alive && !none_left; ++k, pos.advance(S)) {
+        for (int k = 0; k < stages_per_unit; ++k, pos.advance(S)) {
+            if (CLAIM && (!alive || none_left)) break;
             const uint32_t s = pos.stage;
-            if (k > 0 && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
+            if (k > 0 && alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
                 give_up(p, abort_flag);
                 alive = false;
-                break;
             }
             const int g0 = k * G;
             const int g1 = g0 + G < R ? g0 + G : R;
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                 const unsigned char* group = stage + (g - g0) * group_bytes;
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
-                    if (j < n_tok) {
+                    if (U == 1 || j < n_tok) {
                         const unsigned char* row = group + j * rb;
 #pragma unroll
                         for (int jj = 0; jj < NV; ++jj)
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
         }
         // Every row of the unit is in, the residual last: reduce each token's
         // sum of squares (one barrier for the whole unit), then store.
@@ -452,11 +458,15 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
             const float ss = warp_sum(ss2[0] + ss2[1]);
             if (lane == 0) red_unit[j * kConsumerWarps + warp] = ss;
         }
-        if (named_barrier_or(1, kRowsThreads, !alive || none_left)) break;
+        if (CLAIM) {
+            if (named_barrier_or(1, kRowsThreads, !alive || none_left)) break;
+        } else {
+            named_barrier(1, kRowsThreads);
+        }
         red_buf ^= 1;
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-            if (j >= n_tok) break;
+            if (U > 1 && j >= n_tok) break;
             float total = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) total += red_unit[j * kConsumerWarps + w];
@@ -465,7 +475,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
 #pragma unroll
             for (int jj = 0; jj < NV; ++jj) {
                 const int64_t v = static_cast<int64_t>(jj) * kRowsThreads + tid;
-                if (v < nvec) {
+                if (v < nvec && alive) {
                     st_global_cs(static_cast<char*>(p.residual_out) + row_off + v * 16,
                                  V::from_float(x[j][jj]));
                     float w[E], y[E];
@@ -481,40 +491,44 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     }
 }
 
-template <typename T, int NV, int U, bool FLAGS>
+template <typename T, int NV, int U, int MODE>
 void* rows_fn() {
-    return reinterpret_cast<void*>(&rows_kernel<T, NV, U, FLAGS>);
+    return reinterpret_cast<void*>(&rows_kernel<T, NV, U, MODE>);
 }
 
-// The instantiation for a dtype, vectors per thread and unit size (nullptr
-// where U * nv is above kRowsMaxVecs or flags are asked with U > 1).
-template <typename T>
-void* rows_entry_for(int nv, int unit, bool flags) {
-    if (flags) {
-        if (unit != 1) return nullptr;
-        switch (nv) {
-            case 1: return rows_fn<T, 1, 1, true>();
-            case 2: return rows_fn<T, 2, 1, true>();
-            case 3: return rows_fn<T, 3, 1, true>();
-            case 4: return rows_fn<T, 4, 1, true>();
-            default: return nullptr;
-        }
-    }
+// The instantiation for a dtype, vectors per thread, unit size and variant
+// (nullptr where U * nv is above kRowsMaxVecs or flags are asked with U > 1).
+template <typename T, int MODE>
+void* rows_entry_mode(int nv, int unit) {
     switch (nv * 8 + unit) {
-        case 1 * 8 + 1: return rows_fn<T, 1, 1, false>();
-        case 1 * 8 + 2: return rows_fn<T, 1, 2, false>();
-        case 1 * 8 + 4: return rows_fn<T, 1, 4, false>();
-        case 2 * 8 + 1: return rows_fn<T, 2, 1, false>();
-        case 2 * 8 + 2: return rows_fn<T, 2, 2, false>();
-        case 3 * 8 + 1: return rows_fn<T, 3, 1, false>();
-        case 4 * 8 + 1: return rows_fn<T, 4, 1, false>();
+        case 1 * 8 + 1: return rows_fn<T, 1, 1, MODE>();
+        case 2 * 8 + 1: return rows_fn<T, 2, 1, MODE>();
+        case 3 * 8 + 1: return rows_fn<T, 3, 1, MODE>();
+        case 4 * 8 + 1: return rows_fn<T, 4, 1, MODE>();
+        default: break;
+    }
+    if (MODE == kFlags) return nullptr;
+    switch (nv * 8 + unit) {
+        case 1 * 8 + 2: return rows_fn<T, 1, 2, MODE == kFlags ? kFixed : MODE>();
+        case 1 * 8 + 4: return rows_fn<T, 1, 4, MODE == kFlags ? kFixed : MODE>();
+        case 2 * 8 + 2: return rows_fn<T, 2, 2, MODE == kFlags ? kFixed : MODE>();
         default: return nullptr;
     }
 }
 
-void* rows_kernel_for(int dtype, int nv, int unit, bool flags) {
-    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nv, unit, flags)
-                            : rows_entry_for<float>(nv, unit, flags);
+template <typename T>
+void* rows_entry_for(int nv, int unit, int mode) {
+    switch (mode) {
+        case kFixed: return rows_entry_mode<T, kFixed>(nv, unit);
+        case kClaim: return rows_entry_mode<T, kClaim>(nv, unit);
+        case kFlags: return rows_entry_mode<T, kFlags>(nv, unit);
+        default: return nullptr;
+    }
+}
+
+void* rows_kernel_for(int dtype, int nv, int unit, int mode) {
+    return dtype == TW_BF16 ? rows_entry_for<__nv_bfloat16>(nv, unit, mode)
+                            : rows_entry_for<float>(nv, unit, mode);
 }
 
 int rows_vectors_per_thread(int64_t row_bytes) {
@@ -592,8 +606,8 @@ int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
         for (int nv = 1; nv <= kRowsMaxVecs; ++nv)
             for (int unit = 1; unit <= kRowsMaxUnit; unit *= 2)
-                for (bool flags : {false, true}) {
-                    void* fn = rows_kernel_for(dt, nv, unit, flags);
+                for (int mode : {kFixed, kClaim, kFlags}) {
+                    void* fn = rows_kernel_for(dt, nv, unit, mode);
                     if (!fn) continue;
                     cudaError_t e = cudaFuncSetAttribute(
                         fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
@@ -604,8 +618,8 @@ int rows_set_smem_limit(int smem_optin) {
 
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream) {
-    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.unit_tokens,
-                               p.ready != nullptr);
+    const int mode = p.ready ? kFlags : p.work ? kClaim : kFixed;
+    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.unit_tokens, mode);
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
     return launch_with_pdl(fn, p, grid, kRowsBlock, smem_bytes, pdl, stream);
 }

@@ -507,13 +507,15 @@ void* rows_entry_mode(int nv, int unit) {
         case 4 * 8 + 1: return rows_fn<T, 4, 1, MODE>();
         default: break;
     }
-    if (MODE == kFlags) return nullptr;
-    switch (nv * 8 + unit) {
-        case 1 * 8 + 2: return rows_fn<T, 1, 2, MODE == kFlags ? kFixed : MODE>();
-        case 1 * 8 + 4: return rows_fn<T, 1, 4, MODE == kFlags ? kFixed : MODE>();
-        case 2 * 8 + 2: return rows_fn<T, 2, 2, MODE == kFlags ? kFixed : MODE>();
-        default: return nullptr;
+    if constexpr (MODE != kFlags) {
+        switch (nv * 8 + unit) {
+            case 1 * 8 + 2: return rows_fn<T, 1, 2, MODE>();
+            case 1 * 8 + 4: return rows_fn<T, 1, 4, MODE>();
+            case 2 * 8 + 2: return rows_fn<T, 2, 2, MODE>();
+            default: break;
+        }
     }
+    return nullptr;
 }
 
 template <typename T>

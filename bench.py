@@ -324,12 +324,14 @@ def device_leg(res, steps, warmup, max_sms=None, path="auto", sync_ranks=None,
 
 
 # ------------------------------------------------------------------ e2e ---
-def e2e_leg(wl, steps, warmup, chunks=(64, 128, 256, 512), sync_ranks=None):
+def e2e_leg(wl, steps, warmup, chunks=(0, 128, 256, 512), sync_ranks=None):
     """The same step from pinned HOST buffers through the C ABI's host entry
     point (tw_fused_reduce_add_rmsnorm_host): every step moves that step's
-    inputs host->device, runs the kernel and moves the outputs back, with the
-    copies of one token chunk overlapping the kernel on the previous chunk.
-    Returns the best chunk's (ms per step, chunk) and all chunks' ms."""
+    inputs host->device, runs the kernel and moves the outputs back.  Chunk 0:
+    one kernel reads the host tensors in place over the host link and stores
+    straight into the host outputs; chunks >= 1: host->device copies of one
+    token chunk overlap the kernel on the previous chunk.  Returns the best
+    chunk's (ms per step, chunk) and all chunks' ms."""
     import torch
     from reduce_residual_rmsnorm_tw_gb300 import inputs, tw
     d = inputs.make_inputs(wl, device="cuda")
@@ -342,9 +344,9 @@ def e2e_leg(wl, steps, warmup, chunks=(64, 128, 256, 512), sync_ranks=None):
     torch.cuda.synchronize()
     per_chunk = {}
     for chunk in chunks:
-        ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk,
-                                                    wl.torch_dtype),
-                         dtype=torch.uint8, device="cuda")
+        ws = None if chunk == 0 else torch.empty(
+            tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk, wl.torch_dtype),
+            dtype=torch.uint8, device="cuda")
 
         def step():
             tw.tw_fused_reduce_add_rmsnorm_host(h_parts, h_res, h_w, h_out, h_res_out, wl.eps,
@@ -927,10 +929,10 @@ def tw_main(args):
                "link_gbs": round((h2d + d2h) / (step_ms * 1e-3) / 1e9, 1),
                "chunk_tokens": chunk,
                "ms_per_step_by_chunk": {str(k): round(v, 4) for k, v in per_chunk.items()},
-               "path": "tw_fused_reduce_add_rmsnorm_host: pinned host buffers, "
-                       "chunked host->device copies overlapping the kernel on the previous "
-                       "chunk, which stores its results straight into the mapped host "
-                       "outputs (device->host copies where they are not mapped)"}
+               "path": "tw_fused_reduce_add_rmsnorm_host on pinned host buffers: chunk 0 = "
+                       "one kernel reading the host tensors in place over the host link and "
+                       "storing into the host outputs; chunks >= 1 = host->device copies of "
+                       "one chunk overlapping the kernel on the previous chunk"}
     configs = configs_leg(peak) if extra else None
     overlap = overlap_leg() if extra else None
     if args.overlap and rank == 0:

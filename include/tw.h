@@ -224,7 +224,16 @@ int tw_split_launch(const void* const* partials, int n_parts,
 
 /* The fused step for tensors in page-locked HOST memory (cudaHostAlloc or
  * cudaHostRegister): partials, residual, weight, out and residual_out are host
- * pointers with the layout and rules above; only `workspace` is device memory,
+ * pointers with the layout and rules above.
+ * chunk_tokens == 0 (in place): one launch, on `stream`, whose kernel reads
+ * the host tensors through their device mappings and stores straight into the
+ * host outputs (plain loads and stores over the host link: the cluster
+ * kernel).  Every tensor must be mapped into the device's address space
+ * (cudaHostGetDevicePointer succeeds: all page-locked memory on a system with
+ * unified addressing), else TW_ERR_INVALID_ARG; the row must fit the
+ * cluster kernel (H * size <= 8 KB times the cluster size, 64 KB without a
+ * budget), else TW_ERR_UNSUPPORTED.  `workspace` is not used (may be NULL).
+ * chunk_tokens >= 1 (staged): only `workspace` is device memory,
  * at least tw_host_workspace_bytes() bytes, 256-byte aligned, owned by the
  * caller.  Rows [t0, t1) are moved in chunks of chunk_tokens tokens: the
  * host->device copies of one chunk overlap the kernel on the previous one, on
@@ -237,8 +246,8 @@ int tw_split_launch(const void* const* partials, int n_parts,
  * kernel or copy back).  The host buffers and the workspace are in use until
  * the work on `stream` completes.  A chunk_tokens above t1 - t0 is cut to
  * t1 - t0 (the workspace is then checked against that chunk).  Returns
- * TW_ERR_INVALID_ARG if a tensor is not page-locked host memory or the
- * workspace is too small. */
+ * TW_ERR_INVALID_ARG if chunk_tokens < 0, a tensor is not page-locked host
+ * memory or the workspace is too small. */
 int tw_fused_reduce_add_rmsnorm_host(const void* const* partials, int n_parts,
                                      const void* residual, const void* weight,
                                      void* const* out, int n_out,

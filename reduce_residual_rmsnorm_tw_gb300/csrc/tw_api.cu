@@ -169,6 +169,7 @@ struct Args {
     int max_sms;
     int dtype;
     int colsplit = 0;
+    int host_direct = 0;  // tensors in mapped host memory, read in place
     const unsigned int* ready = nullptr;  // readiness flags (rows kernel only)
     int64_t block_tokens = 0;
     unsigned int epoch = 0;
@@ -323,7 +324,9 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
     // max_sms SMs hold its CTAs.
     const bool pdl = a.max_sms >= d.sm_count;
     Params p = make_params(a, d, t0, t1, smid_log);
-    p.prefetch = pdl ? 1 : 0;
+    // L2 warming is for device memory; host-resident rows are read once,
+    // in place.
+    p.prefetch = pdl && !a.host_direct ? 1 : 0;
     // Largest power-of-two cluster within the budget (at most 8: portable).
     int cluster = 1;
     while (cluster * 2 <= 8 && cluster * 2 <= sms) cluster *= 2;
@@ -335,6 +338,9 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
                         "the column-split mode and readiness flags run on the rows kernel only");
         path = TW_PATH_ROWS;
     }
+    // Host-resident tensors are read with plain loads (the cluster kernel):
+    // the rows kernel's bulk copies are kept to device memory.
+    if (a.host_direct) path = TW_PATH_CLUSTER;
     int log2c = 0;
     while ((2 << log2c) <= cluster) ++log2c;
     // Clusters that run at once with every CTA alone on its SM, and (launches
@@ -430,12 +436,58 @@ bool is_pinned_host(const void* p) {
     return attr.type == cudaMemoryTypeHost;
 }
 
+// chunk_tokens == 0: one launch whose kernel reads the host tensors in place
+// and stores straight into the host outputs, through their device mappings.
+int fused_in_place_from_host(const Args& a, void* stream) {
+    if (a.t0 == a.t1) return TW_OK;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != TW_OK) return rc;
+    const void* m_parts[TW_MAX_PARTS];
+    void* m_out[TW_MAX_OUTS];
+    void* m_res = nullptr;
+    void* m_weight = nullptr;
+    void* m_res_out = nullptr;
+    bool mapped = true;
+    for (int r = 0; mapped && r < a.n_parts; ++r) {
+        void* m = nullptr;
+        mapped = is_pinned_host(a.partials[r]) &&
+                 cudaHostGetDevicePointer(&m, const_cast<void*>(a.partials[r]), 0) == cudaSuccess;
+        m_parts[r] = m;
+    }
+    for (int k = 0; mapped && k < a.n_out; ++k)
+        mapped = is_pinned_host(a.out[k]) &&
+                 cudaHostGetDevicePointer(&m_out[k], a.out[k], 0) == cudaSuccess;
+    mapped = mapped && is_pinned_host(a.residual) && is_pinned_host(a.weight) &&
+             is_pinned_host(a.residual_out) &&
+             cudaHostGetDevicePointer(&m_res, const_cast<void*>(a.residual), 0) == cudaSuccess &&
+             cudaHostGetDevicePointer(&m_weight, const_cast<void*>(a.weight), 0) == cudaSuccess &&
+             cudaHostGetDevicePointer(&m_res_out, a.residual_out, 0) == cudaSuccess;
+    if (!mapped) {
+        (void)cudaGetLastError();
+        return fail(TW_ERR_INVALID_ARG,
+                    "chunk_tokens 0 reads the tensors in place: every tensor must be page-locked "
+                    "host memory mapped into the device's address space");
+    }
+    // The alias rules were checked on the host addresses; a mapping keeps
+    // each allocation's bytes contiguous and distinct allocations apart.
+    Args c = a;
+    c.partials = m_parts;
+    c.out = m_out;
+    c.residual = m_res;
+    c.weight = m_weight;
+    c.residual_out = m_res_out;
+    c.host_direct = 1;
+    return launch_range(c, *d, a.t0, a.t1, TW_PATH_CLUSTER, nullptr, stream);
+}
+
 int fused_from_host(const Args& a, void* workspace, size_t workspace_bytes,
                     int64_t chunk_tokens, void* stream) {
     int rc = check_args(a);
     if (rc != TW_OK) return rc;
-    if (chunk_tokens < 1)
-        return fail(TW_ERR_INVALID_ARG, "chunk_tokens %lld < 1", (long long)chunk_tokens);
+    if (chunk_tokens == 0) return fused_in_place_from_host(a, stream);
+    if (chunk_tokens < 0)
+        return fail(TW_ERR_INVALID_ARG, "chunk_tokens %lld < 0", (long long)chunk_tokens);
     // A chunk never needs to be longer than the range; capped so, its bytes
     // stay within a buffer's (at most 2^48, checked above).
     const int64_t span = a.t1 - a.t0 > 1 ? a.t1 - a.t0 : 1;

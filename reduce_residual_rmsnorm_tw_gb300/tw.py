@@ -262,19 +262,22 @@ def tw_host_workspace_bytes(n_parts, n_out, H, chunk_tokens, dtype):
 def tw_fused_reduce_add_rmsnorm_host(partials, residual, weight, out,
                                      residual_out, eps, workspace, chunk_tokens,
                                      t0=0, t1=None, max_sms=None, stream=None):
-    """The fused step on pinned HOST tensors, pipelined in chunks of
-    ``chunk_tokens`` tokens through the device ``workspace`` (a uint8 CUDA
-    tensor of at least tw_host_workspace_bytes bytes)."""
+    """The fused step on pinned HOST tensors.  ``chunk_tokens`` >= 1: pipelined
+    in chunks of that many tokens through the device ``workspace`` (a uint8
+    CUDA tensor of at least tw_host_workspace_bytes bytes).  ``chunk_tokens``
+    == 0: one kernel reads the host tensors in place (``workspace`` may be
+    None)."""
     p_arr, n, o_arr, n_out, T, H, dt = _marshal(partials, residual, weight,
                                                 out, residual_out, on_device=False)
-    if not workspace.is_cuda:
+    if workspace is not None and not workspace.is_cuda:
         raise ValueError("workspace must be a CUDA tensor")
     rc = load().tw_fused_reduce_add_rmsnorm_host(
         p_arr, n, residual.data_ptr(), weight.data_ptr(), o_arr, n_out,
         residual_out.data_ptr(), T, H, eps, t0, T if t1 is None else t1,
-        _ALL_SMS if max_sms is None else max_sms, workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), chunk_tokens,
-        _stream_handle(stream), dt)
+        _ALL_SMS if max_sms is None else max_sms,
+        None if workspace is None else workspace.data_ptr(),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        chunk_tokens, _stream_handle(stream), dt)
     _check(rc)
 
 

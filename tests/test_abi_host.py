@@ -170,7 +170,12 @@ def test_host_entry_workspace_and_argument_checks(lib):
     ws = BASE + 128 * MB
     big = 1 << 30
     f = lib.tw_fused_reduce_add_rmsnorm_host
-    assert f(*args, 0, 4, 8, ws, big, 0, None, 0) == INVALID        # chunk_tokens 0
+    assert f(*args, 0, 4, 8, ws, big, -1, None, 0) == INVALID       # chunk_tokens < 0
+    # chunk_tokens 0 reads the tensors in place (no workspace): with no GPU
+    # the call stops at its first CUDA call, with one at the check that the
+    # fake addresses are mapped host memory.
+    assert f(*args, 0, 4, 8, None, 0, 0, None, 0) in (CUDA, INVALID)
+    assert f(*args, 2, 2, 8, None, 0, 0, None, 0) == OK             # empty range: no-op
     assert f(*args, 0, 4, 8, None, big, 2, None, 0) == INVALID      # no workspace
     assert f(*args, 0, 4, 8, ws + 16, big, 2, None, 0) == ALIGN     # workspace alignment
     assert f(*args, 0, 4, 8, ws, 100, 2, None, 0) == INVALID        # workspace too small

@@ -1,7 +1,7 @@
-"""The host-buffer entry point: pinned host tensors, a device workspace, the
-token range pipelined in chunks.  Checked against the oracle element by
-element, and bit for bit against the device entry point when every chunk
-runs on the same kernel."""
+"""The host-buffer entry point: pinned host tensors, either read in place by
+one kernel (chunk_tokens 0) or pipelined in chunks through a device
+workspace.  Checked against the oracle element by element, and bit for bit
+against the device entry point on the same kernel."""
 import ctypes
 from dataclasses import replace
 
@@ -16,7 +16,16 @@ from tests.parity import SENTINEL, check_close
 pytestmark = pytest.mark.gpu
 
 
-def host_run(wl, chunk, t0=0, t1=None):
+def workspace(wl, chunk):
+    """The device workspace of a staged call (chunk >= 1); none for chunk 0,
+    which reads the host tensors in place."""
+    if chunk == 0:
+        return None
+    nbytes = tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk, wl.torch_dtype)
+    return torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+
+def host_run(wl, chunk, t0=0, t1=None, max_sms=None):
     t1 = wl.T if t1 is None else t1
     d = inputs.make_inputs(wl)
     pin = {"partials": [p.pin_memory() for p in d["partials"]],
@@ -24,10 +33,9 @@ def host_run(wl, chunk, t0=0, t1=None):
     out = [torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
            for _ in range(wl.n_out)]
     res_out = torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()
-    nbytes = tw.tw_host_workspace_bytes(wl.n_parts, wl.n_out, wl.H, chunk, wl.torch_dtype)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     tw.tw_fused_reduce_add_rmsnorm_host(pin["partials"], pin["residual"], pin["weight"], out,
-                                        res_out, wl.eps, ws, chunk, t0, t1)
+                                        res_out, wl.eps, workspace(wl, chunk), chunk, t0, t1,
+                                        max_sms=max_sms)
     torch.cuda.synchronize()
     return d, out, res_out
 
@@ -39,11 +47,13 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("chunk", [1, 7, 33, 64, 1000])
+@pytest.mark.parametrize("chunk,max_sms", [(1, None), (7, None), (33, None), (64, None),
+                                           (1000, None), (0, None), (0, 8)])
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
-def test_host_parity(wl, chunk):
+def test_host_parity(wl, chunk, max_sms):
+    # chunk 0: one kernel reads the host tensors in place.
     t0, t1 = 2, wl.T - 3
-    d, out, res_out = host_run(wl, chunk, t0, t1)
+    d, out, res_out = host_run(wl, chunk, t0, t1, max_sms)
     ref_out, ref_res = oracle.reordered([inputs.to_f64(p) for p in d["partials"]],
                                         inputs.to_f64(d["residual"]), inputs.to_f64(d["weight"]),
                                         wl.eps, n_out=wl.n_out, t0=t0, t1=t1)
@@ -65,6 +75,21 @@ def test_host_matches_device_path_bitwise():
                                       d["weight"].cuda(), dev_out, dev_res, wl.eps, path="rows")
     torch.cuda.synchronize()
     assert torch.equal(out[0], dev_out[0].cpu()) and torch.equal(res_out, dev_res.cpu())
+
+
+def test_host_in_place_matches_device_cluster_path_bitwise():
+    # Reading the host tensors in place runs the cluster kernel over the
+    # mapped memory: the same bits as that kernel on device copies.
+    wl = CASES[0].with_tokens(300)
+    d, out, res_out = host_run(wl, 0)
+    dev_out = [torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")]
+    dev_res = torch.empty(wl.T, wl.H, dtype=wl.torch_dtype, device="cuda")
+    tw.tw_fused_reduce_add_rmsnorm_ex([p.cuda() for p in d["partials"]], d["residual"].cuda(),
+                                      d["weight"].cuda(), dev_out, dev_res, wl.eps,
+                                      path="cluster")
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], dev_out[0].cpu()) and torch.equal(res_out, dev_res.cpu())
+    assert tw.tw_device_status() == 0
 
 
 def test_host_rejects_pageable_memory():
@@ -96,9 +121,10 @@ def test_binding_refuses_tensors_off_the_device():
                                        torch.empty_like(out[0]), wl.eps)
 
 
-def test_host_in_place_residual():
+@pytest.mark.parametrize("chunk", [16, 0])
+def test_host_in_place_residual(chunk):
     # residual_out is the pinned residual itself: each chunk's rows are read
-    # (copied in) before the kernel on that chunk writes them back.
+    # (copied in, or loaded in place) before the kernel writes them back.
     wl = CASES[0]
     t0, t1 = 3, wl.T - 2
     d = inputs.make_inputs(wl)
@@ -106,9 +132,8 @@ def test_host_in_place_residual():
     res = d["residual"].clone().pin_memory()
     w = d["weight"].pin_memory()
     out = [torch.full((wl.T, wl.H), SENTINEL, dtype=wl.torch_dtype).pin_memory()]
-    ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, 1, wl.H, 16, wl.torch_dtype),
-                     dtype=torch.uint8, device="cuda")
-    tw.tw_fused_reduce_add_rmsnorm_host(parts, res, w, out, res, wl.eps, ws, 16, t0, t1)
+    tw.tw_fused_reduce_add_rmsnorm_host(parts, res, w, out, res, wl.eps, workspace(wl, chunk),
+                                        chunk, t0, t1)
     torch.cuda.synchronize()
     ref_out, ref_res = oracle.reordered([inputs.to_f64(p) for p in d["partials"]],
                                         inputs.to_f64(d["residual"]), inputs.to_f64(d["weight"]),
@@ -119,15 +144,15 @@ def test_host_in_place_residual():
                        torch.cat([d["residual"][:t0], d["residual"][t1:]]))
 
 
-def test_host_back_to_back_steps_on_one_stream():
+@pytest.mark.parametrize("chunk", [8, 0])
+def test_host_back_to_back_steps_on_one_stream(chunk):
     # Step 2 reads step 1's host outputs (its partial 0 is step 1's out, its
     # residual step 1's residual_out); enqueued back to back on one stream it
     # must equal the same two steps with the host synchronised between them.
     wl = CASES[0].with_tokens(48)
     d1 = inputs.make_inputs(wl)
     d2 = inputs.make_inputs(replace(wl, seed=wl.seed + 7))
-    ws = torch.empty(tw.tw_host_workspace_bytes(wl.n_parts, 1, wl.H, 8, wl.torch_dtype),
-                     dtype=torch.uint8, device="cuda")
+    ws = workspace(wl, chunk)
     w1, w2 = d1["weight"].pin_memory(), d2["weight"].pin_memory()
     p1 = [p.pin_memory() for p in d1["partials"]]
     rest2 = [p.pin_memory() for p in d2["partials"][1:]]
@@ -139,11 +164,11 @@ def test_host_back_to_back_steps_on_one_stream():
         out2 = [torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()]
         res_out2 = torch.zeros(wl.T, wl.H, dtype=wl.torch_dtype).pin_memory()
         torch.cuda.synchronize()
-        tw.tw_fused_reduce_add_rmsnorm_host(p1, res1, w1, out1, res_out1, wl.eps, ws, 8)
+        tw.tw_fused_reduce_add_rmsnorm_host(p1, res1, w1, out1, res_out1, wl.eps, ws, chunk)
         if sync:
             torch.cuda.synchronize()
         tw.tw_fused_reduce_add_rmsnorm_host([out1[0]] + rest2, res_out1, w2, out2, res_out2,
-                                            wl.eps, ws, 8)
+                                            wl.eps, ws, chunk)
         torch.cuda.synchronize()
         results.append((out2[0].clone(), res_out2.clone()))
     assert torch.equal(results[0][0], results[1][0])

@@ -1,4 +1,5 @@
-// tw_rows.cu -- the rows kernel: persistent CTAs, one token per CTA at a time.
+// tw_rows.cu -- the rows kernel: persistent CTAs, one unit of tokens per CTA
+// at a time.
 //
 // Per token t in [t0, t1) and feature h ("TokenWeave 策略详解", §1 背景 and
 // §5 融合内核):
@@ -9,28 +10,29 @@
 //
 // Layout of the work: a token has R = N + 1 input rows (the N partials, then
 // the residual), each H * b contiguous bytes.  CTAs take UNITS of U
-// consecutive tokens (U = 1, 2 or 4, fixed per launch), unit after unit with
-// a grid stride.  Producer warps stream a unit's rows into a ring of
-// shared-memory stages with 1-D bulk async copies (cp.async.bulk, no tensor
-// map, no multicast): one copy per input buffer and unit covers the U
-// consecutive rows of that buffer (contiguous in a row-major [T, H] tensor),
-// so short rows still move in large copies.  A stage holds `rows_per_stage`
-// such row groups of one unit (the host picks a whole unit when it fits, else
-// an even split of its groups; a stage never crosses into the next unit) and
-// is tracked by a "full" mbarrier (transaction bytes) and an "empty" mbarrier
-// (one arrival per consumer warp).  The ring's stages are dealt round robin to `producers` warps (one
-// elected lane each): the copy rate of one SM grows with the number of
-// warps issuing copies (one issuing warp streamed ~36 GB/s of 16 KB copies
-// whatever the ring depth, two ~69 GB/s), which is what bounds a CTA
-// streaming alone on its SM under a small SM budget.  Whole-row copies keep
-// several large copies from different buffers in flight.  The 512 consumer
+// consecutive tokens (U = 1, 2 or 4, fixed per launch): with a fixed stride,
+// or, in long launches, claimed one by one from a work counter (see the
+// kernel).  Producer warps stream a unit's rows into a ring of shared-memory
+// stages with 1-D bulk async copies (cp.async.bulk, no tensor map, no
+// multicast): one copy per input buffer and unit covers the U consecutive
+// rows of that buffer (contiguous in a row-major [T, H] tensor), so short
+// rows still move in large copies.  A stage holds `rows_per_stage` such row
+// groups of one unit (the host picks a whole unit when it fits, else an even
+// split of its groups; a stage never crosses into the next unit) and is
+// tracked by a "full" mbarrier (transaction bytes) and an "empty" mbarrier
+// (one arrival per consumer warp).  The ring's stages are dealt round robin
+// to `producers` warps (one elected lane each): the copy rate of one SM grows
+// with the number of warps issuing copies (one issuing warp streamed ~36 GB/s
+// of 16 KB copies whatever the ring depth, two ~69 GB/s), which is what bounds
+// a CTA streaming alone on its SM under a small SM budget.  The 512 consumer
 // threads own the 16-byte vectors tid, tid + 512, ... of a row: for each
-// token of the unit they add the staged rows into fp32 registers in row
-// order (ranks first, residual last); after the unit's last stage each
-// token's sum of squares goes through a warp shuffle and the 16 warp totals
-// of every token of the unit through shared memory behind ONE named barrier;
-// then residual_out and the weighted result are stored for each token.  The N-way sum happens while the data
-// streams through shared memory, the counterpart of the pages' sum-at-load.
+// token of the unit they add the staged rows into fp32 registers in row order
+// (ranks first, residual last); after the unit's last stage each token's sum
+// of squares goes through a warp shuffle and the 16 warp totals of every
+// token of the unit through shared memory behind ONE named barrier; then
+// residual_out and the weighted result are stored for each token.  The N-way
+// sum happens while the data streams through shared memory, the counterpart
+// of the pages' sum-at-load.
 //
 // Readiness flags (the FLUX notes' WaitSignal / SetSignal): with a `ready`
 // array, the producer reads no row of token t before ready[t / block_tokens]

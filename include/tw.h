@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define TW_VERSION 10000 /* 1.0.0 */
+#define TW_VERSION 10100 /* 1.1.0: tw_set_ready, in-place host mode, claimed units */
 
 #define TW_MAX_PARTS 16
 #define TW_MAX_OUTS 8

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_error_string(lib):
-    assert tw.tw_version() == 10000
+    assert tw.tw_version() == 10100
     assert isinstance(tw.tw_last_error_string(), str)
 
 

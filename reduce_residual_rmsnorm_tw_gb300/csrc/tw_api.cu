@@ -372,6 +372,7 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
         // schedule.
         if (a.ready || grid < kClaimMinGrid || units < kClaimMinUnits * grid ||
             units >= (int64_t{1} << 31)) {
+            p.pipes = rows_two_pipes_fit(p, a.max_sms < d.sm_count) ? 2 : 1;
             err = launch_rows(p, a.dtype, grid, smem, pdl, stream);
         } else {
             std::lock_guard<std::mutex> lock(d.work_mu);

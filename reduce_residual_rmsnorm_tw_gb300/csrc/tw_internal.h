@@ -69,6 +69,7 @@ struct Params {
     unsigned int epoch;
     int n_parts, n_out;
     int unit_tokens;        // rows kernel: consecutive tokens per unit (1, 2 or 4)
+    int pipes;              // rows kernel: 1, or 2 independent pipelines per CTA
     int rows_per_stage;     // rows kernel: row groups (one buffer's rows of a unit) per stage
     int stages;             // rows kernel: ring depth (a multiple of producers)
     int producers;          // rows kernel: producer warps issuing copies (1..kRowsMaxProducers)
@@ -99,6 +100,9 @@ int rows_unit_tokens(const Params& p, int64_t tokens, int64_t sms);
 // dynamic shared memory to request, or 0 if the rows do not fit in
 // smem_optin bytes.
 size_t rows_plan(Params& p, int smem_optin);
+// Whether the launch planned in p (fixed schedule, unit size and ring set)
+// runs as two pipelines per CTA (`budgeted`: held below the SM count).
+bool rows_two_pipes_fit(const Params& p, bool budgeted);
 // Raise the dynamic shared memory limit of every kernel instantiation on the
 // current device (cudaError_t as int).
 int rows_set_smem_limit(int smem_optin);

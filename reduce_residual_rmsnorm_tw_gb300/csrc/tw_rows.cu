@@ -54,7 +54,9 @@ constexpr int kConsumerWarps = kRowsThreads / 32;
 constexpr int kFullOff = 0;
 constexpr int kEmptyOff = 8 * kMaxStages;
 constexpr int kRedOff = 16 * kMaxStages;
-constexpr int kAbortOff = kRedOff + 2 * kRowsMaxUnit * kConsumerWarps * 4;
+// Warp totals of the sum of squares: double-buffered, U tokens x 16 warps,
+// for each of the two consumer groups of the two-pipeline variant.
+constexpr int kAbortOff = kRedOff + 2 * 2 * kRowsMaxUnit * kConsumerWarps * 4;
 // Claimed-unit bookkeeping: the unit index each stage carries, the queue of
 // claimed units producer 0 hands producer 1 ((unit, tag) pairs), and the last
 // queue position producer 1 has read.
@@ -62,7 +64,7 @@ constexpr int kUnitQueue = 4;
 constexpr int kStageUnitOff = kAbortOff + 8;
 constexpr int kQueueOff = kStageUnitOff + 8 * kMaxStages;
 constexpr int kSeenOff = kQueueOff + 16 * kUnitQueue;
-constexpr int kRingOff = 1024;
+constexpr int kRingOff = 2048;
 // Tokens of its own a CTA prefetches into L2 before its first global read
 // (three measured best), never more than kPrefetchMaxBytes, so the prefetch
 // of a whole grid stays well inside L2.
@@ -535,8 +537,271 @@ void* rows_kernel_for(int dtype, int nv, int unit, int mode) {
                             : rows_entry_for<float>(nv, unit, mode);
 }
 
-int rows_vectors_per_thread(int64_t row_bytes) {
-    return static_cast<int>((row_bytes / 16 + kRowsThreads - 1) / kRowsThreads);
+// Two pipelines per CTA (fixed schedule only).  The CTA's ring is cut into
+// two halves, each with its own producer warp, its own 8 consumer warps and
+// its own stages and mbarriers; pipeline g takes the CTA's units at
+// positions g, g + 2, g + 4, ... (unit b + i * grid at position i).  Each
+// pipeline walks only its own slots in order, so no wait can mistake an
+// older phase of a slot for the one it needs.  A consumer group's chain of
+// "wait for a stage, read it, release it" then runs beside the other
+// group's, and a stage that lands while one group is in its epilogue is
+// taken by the other.  Per unit the group meets at its own named barrier
+// (ids 1 and 2, 256 threads each).  NV: vectors per consumer thread and row
+// with 256 threads per group (U * NV <= kRowsMaxVecs).
+template <typename T, int NV, int U>
+__global__ void __launch_bounds__(kRowsBlock, 1)
+    rows2_kernel(const __grid_constant__ Params p) {
+    static_assert(U >= 1 && U <= kRowsMaxUnit && U * NV <= kRowsMaxVecs, "unit too large");
+    constexpr int kGroupWarps = kConsumerWarps / 2;
+    constexpr int kGroupThreads = kRowsThreads / 2;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    using V = Vec<T>;
+    constexpr int E = V::kElems;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t S = static_cast<uint32_t>(p.stages);  // even: S / 2 per pipeline
+    const uint32_t Sg = S / 2;
+    const int n_sum = p.colsplit ? 1 : p.n_parts;
+    const int R = n_sum + 1;
+    const int G = p.rows_per_stage;
+    const int stages_per_unit = (R + G - 1) / G;
+    const int64_t rb = p.row_bytes;
+    const uint32_t group_bytes = static_cast<uint32_t>(U * rb);
+    const uint32_t stage_bytes = static_cast<uint32_t>(G) * group_bytes;
+    const uint32_t full0 = smem_addr(smem + kFullOff);
+    const uint32_t empty0 = smem_addr(smem + kEmptyOff);
+    float* red = reinterpret_cast<float*>(smem + kRedOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+    const unsigned char* ring = smem + kRingOff;
+    const uint32_t ring_addr = smem_addr(ring);
+    const int64_t n_units = (p.t1 - p.t0 + U - 1) / U;
+
+    if (tid == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kGroupWarps);
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    // L2 warming before the dependency wait, as in rows_kernel.
+    if (warp == kConsumerWarps && lane == 0 && p.prefetch) {
+        const int64_t unit_bytes = static_cast<int64_t>(R) * U * rb;
+        int64_t n_pre = (kPrefetchTokens + U - 1) / U;
+        if (n_pre * unit_bytes > kPrefetchMaxBytes) n_pre = kPrefetchMaxBytes / unit_bytes;
+        for (int64_t i = 0; i < n_pre; ++i) {
+            const int64_t u = blockIdx.x + i * gridDim.x;
+            if (u >= n_units) break;
+            const int64_t t = p.t0 + u * U;
+            const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
+            prefetch_tokens(p, t, n_tok, R, n_sum);
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (tid == 0 && p.smid_log) p.smid_log[blockIdx.x] = sm_id();
+
+    if (warp >= kConsumerWarps) {
+        // ------------------------------------------------------ producers ---
+        const int pw = warp - kConsumerWarps;  // pipeline
+        if (lane != 0 || pw >= 2) return;
+        const uint64_t pol = policy_evict_first();
+        const uint32_t base = static_cast<uint32_t>(pw) * Sg;
+        RingPos pos;
+        uint64_t issued = 0;
+        bool stop = false;
+        for (int64_t i = pw; !stop; i += 2) {
+            const int64_t u = blockIdx.x + i * gridDim.x;
+            if (u >= n_units) break;
+            const int64_t t = p.t0 + u * U;
+            const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
+            const uint32_t copy_bytes = static_cast<uint32_t>(n_tok * rb);
+            const int64_t row_off = t * rb;
+            for (int k = 0; k < stages_per_unit; ++k, ++issued, pos.advance(Sg)) {
+                const uint32_t s = base + pos.stage;
+                if (*abort_flag ||
+                    (issued >= Sg && !mbar_wait(empty0 + 8 * s, pos.phase ^ 1u, abort_flag))) {
+                    give_up(p, abort_flag);
+                    stop = true;
+                    break;
+                }
+                const int g0 = k * G;
+                const int g1 = g0 + G < R ? g0 + G : R;
+                const uint32_t bar = full0 + 8 * s;
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(g1 - g0) * copy_bytes);
+                uint32_t dst = ring_addr + s * stage_bytes;
+                for (int g = g0; g < g1; ++g, dst += group_bytes) {
+                    if (g == n_sum) {
+                        bulk_g2s(dst, static_cast<const char*>(p.residual) + row_off, copy_bytes,
+                                 bar, pol);
+                    } else if (p.colsplit) {
+                        for (int j = 0; j < n_tok; ++j)
+                            for (int r = 0; r < p.n_parts; ++r) {
+                                const int64_t lo = p.col_lo[r], hi = p.col_lo[r + 1];
+                                if (lo < hi)
+                                    bulk_g2s(dst + static_cast<uint32_t>(j * rb + lo),
+                                             static_cast<const char*>(p.partials[r]) + row_off +
+                                                 j * rb + lo,
+                                             static_cast<uint32_t>(hi - lo), bar, pol);
+                            }
+                    } else {
+                        bulk_g2s(dst, static_cast<const char*>(p.partials[g]) + row_off,
+                                 copy_bytes, bar, pol);
+                    }
+                }
+            }
+        }
+        // Drain: this pipeline's copies must have landed before the CTA exits.
+        RingPos back = pos;
+        for (uint32_t k = 0; k < Sg && k < issued; ++k) {
+            if (back.stage == 0) {
+                back.stage = Sg - 1;
+                back.phase ^= 1u;
+            } else {
+                --back.stage;
+            }
+            if (!mbar_wait(full0 + 8 * (base + back.stage), back.phase, nullptr))
+                atomicOr(p.status, 2u);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers ---
+    const int grp = warp / kGroupWarps;
+    const int gwarp = warp - grp * kGroupWarps;
+    const int gtid = tid - grp * kGroupThreads;
+    const uint32_t base = static_cast<uint32_t>(grp) * Sg;
+    const int64_t nvec = rb / 16;
+    uint4 wv[NV];
+#pragma unroll
+    for (int jj = 0; jj < NV; ++jj) {
+        const int64_t v = static_cast<int64_t>(jj) * kGroupThreads + gtid;
+        wv[jj] = v < nvec ? ld_global_nc(static_cast<const char*>(p.weight) + v * 16)
+                          : make_uint4(0, 0, 0, 0);
+    }
+    // Bounded waits; a consumer that gave up keeps walking its group's units
+    // (no waits, no stores) so the group's barrier sequence stays whole.
+    RingPos pos;
+    int red_buf = 0;
+    bool alive = true;
+    for (int64_t i = grp;; i += 2) {
+        const int64_t u = blockIdx.x + i * gridDim.x;
+        if (u >= n_units) break;
+        const int64_t t = p.t0 + u * U;
+        const int n_tok = U == 1 ? 1 : (p.t1 - t < U ? static_cast<int>(p.t1 - t) : U);
+        float x[U][NV][E];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj)
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[j][jj][e] = 0.f;
+        for (int k = 0; k < stages_per_unit; ++k, pos.advance(Sg)) {
+            const uint32_t s = base + pos.stage;
+            if (alive && !mbar_wait(full0 + 8 * s, pos.phase, abort_flag)) {
+                give_up(p, abort_flag);
+                alive = false;
+            }
+            const int g0 = k * G;
+            const int g1 = g0 + G < R ? g0 + G : R;
+            const unsigned char* stage = ring + s * stage_bytes + gtid * 16;
+            for (int g = g0; g < g1; ++g) {
+                const unsigned char* group = stage + (g - g0) * group_bytes;
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    if (U == 1 || j < n_tok) {
+                        const unsigned char* row = group + j * rb;
+#pragma unroll
+                        for (int jj = 0; jj < NV; ++jj)
+                            if (static_cast<int64_t>(jj) * kGroupThreads + gtid < nvec)
+                                add_vec(x[j][jj],
+                                        *reinterpret_cast<const uint4*>(
+                                            row + jj * kGroupThreads * 16),
+                                        static_cast<T*>(nullptr));
+                    }
+                }
+            }
+            __syncwarp();
+            if (alive && lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // The sum of squares is reduced exactly as rows_kernel reduces it, so
+        // both kernels give the same bits: vector jj * 256 + gtid belongs, in
+        // rows_kernel, to thread (jj & 1) * 256 + gtid (its vector jj >> 1),
+        // i.e. to warp gwarp (even jj) or gwarp + 8 (odd jj).  Each thread
+        // keeps the two partials apart, each group warp yields the totals of
+        // those two warps, and the 16 totals are added in warp order.
+        float* red_unit = red + (grp * 2 + red_buf) * (U * kConsumerWarps);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            float ev2[2] = {0.f, 0.f}, od2[2] = {0.f, 0.f};
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj)
+                if (static_cast<int64_t>(jj) * kGroupThreads + gtid < nvec) {
+                    if ((jj & 1) == 0)
+                        sum_squares<E>(ev2, x[j][jj]);
+                    else
+                        sum_squares<E>(od2, x[j][jj]);
+                }
+            const float ev = warp_sum(ev2[0] + ev2[1]);
+            const float od = warp_sum(od2[0] + od2[1]);
+            if (lane == 0) {
+                red_unit[j * kConsumerWarps + gwarp] = ev;
+                red_unit[j * kConsumerWarps + kGroupWarps + gwarp] = od;
+            }
+        }
+        named_barrier(1 + grp, kGroupThreads);
+        red_buf ^= 1;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            if (U > 1 && j >= n_tok) break;
+            float total = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) total += red_unit[j * kConsumerWarps + w];
+            const float inv = rsqrtf(total * p.inv_H + p.eps);
+            const int64_t row_off = (t + j) * rb;
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj) {
+                const int64_t v = static_cast<int64_t>(jj) * kGroupThreads + gtid;
+                if (v < nvec && alive) {
+                    st_global_cs(static_cast<char*>(p.residual_out) + row_off + v * 16,
+                                 V::from_float(x[j][jj]));
+                    float w[E], y[E];
+                    V::to_float(wv[jj], w);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) y[e] = (x[j][jj][e] * inv) * w[e];
+                    const uint4 packed = V::from_float(y);
+                    for (int k = 0; k < p.n_out; ++k)
+                        st_global_cs(static_cast<char*>(p.out[k]) + row_off + v * 16, packed);
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+void* rows2_entry_for(int nv, int unit) {
+    switch (nv * 8 + unit) {
+        case 1 * 8 + 1: return reinterpret_cast<void*>(&rows2_kernel<T, 1, 1>);
+        case 2 * 8 + 1: return reinterpret_cast<void*>(&rows2_kernel<T, 2, 1>);
+        case 3 * 8 + 1: return reinterpret_cast<void*>(&rows2_kernel<T, 3, 1>);
+        case 4 * 8 + 1: return reinterpret_cast<void*>(&rows2_kernel<T, 4, 1>);
+        case 1 * 8 + 2: return reinterpret_cast<void*>(&rows2_kernel<T, 1, 2>);
+        case 1 * 8 + 4: return reinterpret_cast<void*>(&rows2_kernel<T, 1, 4>);
+        case 2 * 8 + 2: return reinterpret_cast<void*>(&rows2_kernel<T, 2, 2>);
+        default: return nullptr;
+    }
+}
+
+void* rows2_kernel_for(int dtype, int nv, int unit) {
+    return dtype == TW_BF16 ? rows2_entry_for<__nv_bfloat16>(nv, unit)
+                            : rows2_entry_for<float>(nv, unit);
+}
+
+int rows_vectors_per_thread(int64_t row_bytes, int threads = kRowsThreads) {
+    return static_cast<int>((row_bytes / 16 + threads - 1) / threads);
 }
 
 // Tokens of the busiest CTA when `tokens` tokens are cut into units of u
@@ -606,6 +871,23 @@ size_t rows_plan(Params& p, int smem_optin) {
     return smem < static_cast<size_t>(kExclusiveSmemBytes) ? kExclusiveSmemBytes : smem;
 }
 
+bool rows_two_pipes_fit(const Params& p, bool budgeted) {
+    // Two pipelines: the fixed schedule, at least two ring stages each, and a
+    // unit's x in registers with 256 threads per group.  Under an SM budget
+    // they always pay (8 SMs: 291 -> 266 us on N = 8, H = 8192; 190 -> 156
+    // us on N = 2, H = 4096).  With the whole GPU only when a pipeline's half
+    // of the ring holds a whole unit (N = 2: 14.3 -> 13.6 us); otherwise
+    // each pipeline would wait for its own first stage to be read before it
+    // could fetch a unit's last one (N = 8: 28.2 -> 28.6 us).
+    const int nv2 = rows_vectors_per_thread(p.row_bytes, kRowsThreads / 2);
+    if (p.ready || p.work || p.stages < 4 || p.unit_tokens * nv2 > kRowsMaxVecs ||
+        rows2_kernel_for(TW_BF16, nv2, p.unit_tokens) == nullptr)
+        return false;
+    const int rows = p.colsplit ? 2 : p.n_parts + 1;
+    const int stages_per_unit = (rows + p.rows_per_stage - 1) / p.rows_per_stage;
+    return budgeted || stages_per_unit <= p.stages / 2;
+}
+
 int rows_set_smem_limit(int smem_optin) {
     for (int dt = 0; dt < 2; ++dt)
         for (int nv = 1; nv <= kRowsMaxVecs; ++nv)
@@ -617,13 +899,28 @@ int rows_set_smem_limit(int smem_optin) {
                         fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
                     if (e != cudaSuccess) return static_cast<int>(e);
                 }
+    for (int dt = 0; dt < 2; ++dt)
+        for (int nv = 1; nv <= kRowsMaxVecs; ++nv)
+            for (int unit = 1; unit <= kRowsMaxUnit; unit *= 2) {
+                void* fn = rows2_kernel_for(dt, nv, unit);
+                if (!fn) continue;
+                cudaError_t e = cudaFuncSetAttribute(
+                    fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+                if (e != cudaSuccess) return static_cast<int>(e);
+            }
     return 0;
 }
 
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream) {
-    const int mode = p.ready ? kFlags : p.work ? kClaim : kFixed;
-    void* fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.unit_tokens, mode);
+    void* fn;
+    if (p.pipes == 2) {
+        fn = rows2_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes, kRowsThreads / 2),
+                              p.unit_tokens);
+    } else {
+        const int mode = p.ready ? kFlags : p.work ? kClaim : kFixed;
+        fn = rows_kernel_for(dtype, rows_vectors_per_thread(p.row_bytes), p.unit_tokens, mode);
+    }
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
     return launch_with_pdl(fn, p, grid, kRowsBlock, smem_bytes, pdl, stream);
 }

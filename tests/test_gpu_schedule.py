@@ -4,7 +4,10 @@ its own (faster SMs take more); other launches, and every launch captured
 into a CUDA graph, keep the fixed schedule (CTA b takes units b, b + grid,
 ...).  Either way every token is processed exactly once
 and its result does not depend on which CTA processed it: both are checked
-bit for bit against each other and against the oracle, with many launches
+bit for bit against each other and against the oracle (the fixed launches
+here take the two-pipeline variant, which a budget or a unit that fits half
+the ring selects, while claimed units always run one pipeline, so the
+comparison also holds the two variants to the same bits), with many launches
 in flight at once on several streams (each needs a counter of its own) and
 with more launches in a row than the library holds counters."""
 import pytest

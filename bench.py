@@ -966,12 +966,19 @@ def tw_main(args):
                     "note": "diagnostic pass with an event pair around every launch "
                             "(adds the launch gap, disables launch overlap)"}}
     if foreign:
+        # Strict case: after a kernel that shares nothing with it.  After the
+        # GEMM a layer runs before this step the figure is a marginal time
+        # (part of the launch overlaps the GEMM's end and the GEMM's output,
+        # partial 0, is partly read from L2), not a bandwidth.
         roofline["frac_after_foreign_kernel"] = foreign["spin"]["frac"]
+        roofline["frac_after_gemm_marginal"] = foreign["gemm"]["frac"]
         roofline["after_foreign_kernel"] = foreign
         roofline["after_foreign_kernel_note"] = (
             "fused launch right after a different kernel: [foreign, fused] pairs minus the "
-            "foreign kernels alone; spin = a one-thread spin touching no memory, gemm = a bf16 "
-            "GEMM writing partial 0 of the batch the fused launch reads")
+            "foreign kernels alone; spin = a one-thread spin touching no memory "
+            "(frac_after_foreign_kernel), gemm = a bf16 GEMM writing partial 0 of the batch "
+            "the fused launch reads (frac_after_gemm_marginal: the launch's marginal cost in "
+            "the pair, partly hidden behind the GEMM's end)")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,

@@ -537,6 +537,20 @@ void* rows_kernel_for(int dtype, int nv, int unit, int mode) {
                             : rows_entry_for<float>(nv, unit, mode);
 }
 
+// y[0..1] = (x[0..1] * inv) * w[0..1], two lanes per instruction (each lane
+// rounds as the scalar multiplies do).
+__device__ __forceinline__ void scale2(float* y, const float* x, float inv, const float* w) {
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %4};\n\t"
+        "mul.rn.f32x2 a, a, b;\n\t"
+        "mov.b64 c, {%5, %6};\n\t"
+        "mul.rn.f32x2 a, a, c;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "=f"(y[0]), "=f"(y[1])
+        : "f"(x[0]), "f"(x[1]), "f"(inv), "f"(w[0]), "f"(w[1]));
+}
+
 // Two pipelines per CTA (fixed schedule only).  The CTA's ring is cut into
 // two halves, each with its own producer warp, its own 8 consumer warps and
 // its own stages and mbarriers; pipeline g takes the CTA's units at
@@ -687,6 +701,10 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
     RingPos pos;
     int red_buf = 0;
     bool alive = true;
+    int nv_ok = 0;  // vectors of a row this thread owns
+#pragma unroll
+    for (int jj = 0; jj < NV; ++jj)
+        if (static_cast<int64_t>(jj) * kGroupThreads + gtid < nvec) nv_ok = jj + 1;
     for (int64_t i = grp;; i += 2) {
         const int64_t u = blockIdx.x + i * gridDim.x;
         if (u >= n_units) break;
@@ -716,7 +734,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                         const unsigned char* row = group + j * rb;
 #pragma unroll
                         for (int jj = 0; jj < NV; ++jj)
-                            if (static_cast<int64_t>(jj) * kGroupThreads + gtid < nvec)
+                            if (jj < nv_ok)
                                 add_vec(x[j][jj],
                                         *reinterpret_cast<const uint4*>(
                                             row + jj * kGroupThreads * 16),
@@ -758,8 +776,15 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
         for (int j = 0; j < U; ++j) {
             if (U > 1 && j >= n_tok) break;
             float total = 0.f;
+            const float4* r4 = reinterpret_cast<const float4*>(red_unit + j * kConsumerWarps);
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) total += red_unit[j * kConsumerWarps + w];
+            for (int w4 = 0; w4 < kConsumerWarps / 4; ++w4) {
+                const float4 q4 = r4[w4];
+                total += q4.x;
+                total += q4.y;
+                total += q4.z;
+                total += q4.w;
+            }
             const float inv = rsqrtf(total * p.inv_H + p.eps);
             const int64_t row_off = (t + j) * rb;
 #pragma unroll
@@ -771,7 +796,7 @@ __global__ void __launch_bounds__(kRowsBlock, 1)
                     float w[E], y[E];
                     V::to_float(wv[jj], w);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) y[e] = (x[j][jj][e] * inv) * w[e];
+                    for (int e = 0; e < E; e += 2) scale2(y + e, x[j][jj] + e, inv, w + e);
                     const uint4 packed = V::from_float(y);
                     for (int k = 0; k < p.n_out; ++k)
                         st_global_cs(static_cast<char*>(p.out[k]) + row_off + v * 16, packed);

@@ -109,6 +109,26 @@ def test_colsplit_sub_range_in_place():
     check_workload(COLSPLIT[0], colsplit=True, t0=5, t1=30, in_place=True)
 
 
+# Several units per CTA under a budget (the two-pipeline variant of the rows
+# kernel, whose consumer groups take alternate units): fp32 rows of 20 KB in
+# one-token units, bf16 rows of 8 KB in units of two tokens, a ragged tail.
+COLSPLIT_BUDGET = [
+    (wl(4, 67, 5120, "f32", n_out=2, column=True), 3),
+    (wl(2, 203, 4096, column=True), 8),
+    (wl(8, 61, 2048, column=True), 5),
+]
+
+
+@pytest.mark.parametrize("case", COLSPLIT_BUDGET, ids=lambda c: f"{c[0].name}_sms{c[1]}")
+def test_colsplit_under_budget(case):
+    w, sms = case
+    out, res = check_workload(w, colsplit=True, max_sms=sms)
+    dense_out, dense_res = check_workload(w, path="rows", max_sms=sms)
+    for a, b in zip(out + [res], dense_out + [dense_res]):
+        assert torch.equal(a, b), "column-split result differs from the dense rows kernel"
+    check_workload(w, colsplit=True, max_sms=sms, t0=3, t1=w.T - 2, in_place=True)
+
+
 def test_parity_traditional_order():
     check_workload(CASES[3], order="traditional")
 

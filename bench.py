@@ -227,11 +227,12 @@ class Resident:
 
 def time_launches(launchers, steps, warmup, stream, sync_ranks=None, per_launch=False):
     """Launch launchers[i % n] for warmup + steps steps on `stream` and time
-    the steps with CUDA events around the region; the average launch is the
-    region divided by the steps (the launches run back to back, each may
-    overlap its start with the previous one's drain).  With per_launch=True
-    every launch is also bracketed by its own events (a diagnostic: events
-    between kernels add the launch gap to every step).
+    the steps with CUDA events around the region (a spin kernel queued just
+    before the start event covers the host's enqueue time); the average
+    launch is the region divided by the steps (the launches run back to back,
+    each may overlap its start with the previous one's drain).  With
+    per_launch=True every launch is also bracketed by its own events (a
+    diagnostic: events between kernels add the launch gap to every step).
     Returns (region_ms, per_launch_ms list or None)."""
     import torch
     n = len(launchers)
@@ -250,6 +251,11 @@ def time_launches(launchers, steps, warmup, stream, sync_ranks=None, per_launch=
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("tw_timed")  # lets ncu --nvtx-include select this region
     with torch.cuda.stream(stream):
+        # A ~50 us spin ahead of the start event keeps the stream busy while
+        # the host enqueues the event and the first launches, so the region
+        # holds device time only (not the host's time to issue the first
+        # launch).  The first timed launch still follows a foreign kernel.
+        torch.cuda._sleep(100_000)
         begin.record(stream)
         if per_launch:
             for i in range(steps):

@@ -95,7 +95,7 @@ typedef enum {
 
 /* Kernel choice for tw_fused_reduce_add_rmsnorm_ex. */
 typedef enum {
-    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 64 tokens whose
+    TW_PATH_AUTO = 0,  /* cluster kernel for ranges of at most 128 tokens whose
                           clusters (one per token) can all run at once on the
                           device, when the row fits a cluster; rows kernel
                           otherwise */

@@ -48,10 +48,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 // on this GPU (one warp cannot pull a 100+ KB token quickly) and runs only
 // when asked for.
 constexpr int64_t kClusterPathMaxTokens = 8;
-// AUTO never takes the cluster kernel beyond this many tokens (measured: at
-// 64 tokens it still beat the rows kernel, 4.1 vs 4.4 us; at 256 it lost,
-// 14.7 vs 9.5 us).
-constexpr int64_t kClusterAutoMaxTokens = 64;
+// AUTO never takes the cluster kernel beyond this many tokens (measured on
+// N = 8, H = 8192 bf16: at 128 tokens it still beat the rows kernel, 5.65
+// vs 5.8 us; at 152 it lost, 8.1 vs 6.6 us).
+constexpr int64_t kClusterAutoMaxTokens = 128;
 // Rows launches claim units from a work counter when they have at least this
 // many CTAs and units per CTA (on a GB300 this took the 8192- and 16384-token
 // workloads 5-10 % faster; launches of ~7 units per CTA or on a few SMs gained

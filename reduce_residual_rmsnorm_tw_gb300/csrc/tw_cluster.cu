@@ -62,7 +62,12 @@ __device__ __forceinline__ void st_peer_f32(float* local, uint32_t rank, float v
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <typename T, int VPT>
+// VPT: 16-byte vectors per thread and row; NP: partial rows held in
+// registers at once (the smallest of 2, 4, 8, 16 that covers n_parts), so
+// that a launch with few partials keeps few registers and more CTAs fit on
+// an SM (N = 8 bf16 rows of 16 KB: 62 registers, 8 CTAs per SM, against 95
+// and 5 when every launch reserved room for 16).
+template <typename T, int VPT, int NP>
 __global__ void __launch_bounds__(kClusterThreads)
     cluster_kernel(const __grid_constant__ Params p) {
     using V = Vec<T>;
@@ -115,15 +120,24 @@ __global__ void __launch_bounds__(kClusterThreads)
     int buf = 0;
     for (int64_t t = p.t0 + cluster_index(); t < p.t1; t += cluster_count()) {
         const int64_t row_off = t * p.row_bytes;
+        // Warm L2 with this CTA's slice of the cluster's next token, so that
+        // its loads overlap this token's reduction and stores.
+        if (tid == 0 && p.prefetch && v_begin < v_end && t + cluster_count() < p.t1) {
+            const int64_t off = (t + cluster_count()) * p.row_bytes + v_begin * 16;
+            const uint32_t bytes = static_cast<uint32_t>((v_end - v_begin) * 16);
+            for (int r = 0; r < p.n_parts; ++r)
+                bulk_prefetch_l2(static_cast<const char*>(p.partials[r]) + off, bytes);
+            bulk_prefetch_l2(static_cast<const char*>(p.residual) + off, bytes);
+        }
         float x[VPT][E];
         float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int64_t v = v_begin + tid + k * kClusterThreads;
             const bool valid = v < v_end;
-            uint4 raw[TW_MAX_PARTS];
+            uint4 raw[NP];
 #pragma unroll
-            for (int r = 0; r < TW_MAX_PARTS; ++r)
+            for (int r = 0; r < NP; ++r)
                 raw[r] = (valid && r < p.n_parts)
                              ? ld_global_nc(static_cast<const char*>(p.partials[r]) + row_off +
                                             v * 16)
@@ -134,7 +148,7 @@ __global__ void __launch_bounds__(kClusterThreads)
 #pragma unroll
             for (int e = 0; e < E; ++e) x[k][e] = 0.f;
 #pragma unroll
-            for (int r = 0; r < TW_MAX_PARTS; ++r) {
+            for (int r = 0; r < NP; ++r) {
                 if (r < p.n_parts) {
                     float f[E];
                     V::to_float(raw[r], f);
@@ -196,18 +210,38 @@ __global__ void __launch_bounds__(kClusterThreads)
     if (!peers_started) cluster_wait();
 }
 
-template <typename T>
-void* cluster_entry_for(int vpt) {
+template <typename T, int NP>
+void* cluster_entry_np(int vpt) {
     switch (vpt) {
-        case 1: return reinterpret_cast<void*>(&cluster_kernel<T, 1>);
-        case 2: return reinterpret_cast<void*>(&cluster_kernel<T, 2>);
-        case 4: return reinterpret_cast<void*>(&cluster_kernel<T, 4>);
+        case 1: return reinterpret_cast<void*>(&cluster_kernel<T, 1, NP>);
+        case 2: return reinterpret_cast<void*>(&cluster_kernel<T, 2, NP>);
+        case 4: return reinterpret_cast<void*>(&cluster_kernel<T, 4, NP>);
         default: return nullptr;
     }
 }
 
-void* cluster_kernel_for(int dtype, int vpt) {
-    return dtype == TW_BF16 ? cluster_entry_for<__nv_bfloat16>(vpt) : cluster_entry_for<float>(vpt);
+template <typename T>
+void* cluster_entry_for(int vpt, int np) {
+    switch (np) {
+        case 2: return cluster_entry_np<T, 2>(vpt);
+        case 4: return cluster_entry_np<T, 4>(vpt);
+        case 8: return cluster_entry_np<T, 8>(vpt);
+        case 16: return cluster_entry_np<T, 16>(vpt);
+        default: return nullptr;
+    }
+}
+
+// Partials held in registers per thread: the smallest of 2, 4, 8, 16 that
+// covers n_parts.
+int cluster_np(int n_parts) {
+    int np = 2;
+    while (np < n_parts) np *= 2;
+    return np;
+}
+
+void* cluster_kernel_for(int dtype, int vpt, int np) {
+    return dtype == TW_BF16 ? cluster_entry_for<__nv_bfloat16>(vpt, np)
+                            : cluster_entry_for<float>(vpt, np);
 }
 
 }  // namespace
@@ -226,12 +260,13 @@ int cluster_set_attributes(int smem_optin) {
     // request stays at the exclusive-SM amount, not the full opt-in limit.
     if (smem_optin < kExclusiveSmemBytes + 1024) return static_cast<int>(cudaErrorInvalidValue);
     for (int dt = 0; dt < 2; ++dt)
-        for (int v = 1; v <= kClusterMaxVpt; v *= 2) {
-            cudaError_t e = cudaFuncSetAttribute(cluster_kernel_for(dt, v),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kExclusiveSmemBytes);
-            if (e != cudaSuccess) return static_cast<int>(e);
-        }
+        for (int v = 1; v <= kClusterMaxVpt; v *= 2)
+            for (int np = 2; np <= 16; np *= 2) {
+                cudaError_t e = cudaFuncSetAttribute(cluster_kernel_for(dt, v, np),
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     kExclusiveSmemBytes);
+                if (e != cudaSuccess) return static_cast<int>(e);
+            }
     return 0;
 }
 
@@ -250,13 +285,13 @@ int cluster_max_active(int cluster, size_t smem_bytes, int* n) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return static_cast<int>(
-        cudaOccupancyMaxActiveClusters(n, cluster_kernel_for(TW_BF16, 1), &cfg));
+        cudaOccupancyMaxActiveClusters(n, cluster_kernel_for(TW_BF16, 1, 8), &cfg));
 }
 
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
                    bool pdl, void* stream) {
     const int vpt = cluster_vectors_per_thread(p.row_bytes, cluster);
-    void* fn = cluster_kernel_for(dtype, vpt);
+    void* fn = cluster_kernel_for(dtype, vpt, cluster_np(p.n_parts));
     if (!fn) return static_cast<int>(cudaErrorInvalidValue);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster * n_clusters));

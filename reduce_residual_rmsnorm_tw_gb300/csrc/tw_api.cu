@@ -394,7 +394,11 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
     } else if (path == TW_PATH_WARP) {
         const int64_t ctas = (tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta;
         const int grid = static_cast<int>(ctas < sms ? ctas : sms);
-        err = launch_warp(p, a.dtype, grid, kExclusiveSmemBytes, pdl, stream);
+        const size_t xs = warp_stage_bytes(p.row_bytes, a.dtype);
+        const bool staged = xs <= static_cast<size_t>(d.smem_optin);
+        const size_t smem =
+            staged && xs > static_cast<size_t>(kExclusiveSmemBytes) ? xs : kExclusiveSmemBytes;
+        err = launch_warp(p, a.dtype, grid, smem, staged, pdl, stream);
     } else if (path == TW_PATH_CLUSTER) {
         if (!d.cluster_ready)
             return fail(TW_ERR_UNSUPPORTED, "cluster kernel unavailable on this device (%s)",

@@ -88,7 +88,10 @@ int set_last_error(int code, const char* message);
 // first global memory access.
 int launch_rows(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
                 void* stream);
-int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool pdl,
+// Shared memory the warp kernel needs to keep every warp's token x between
+// its two passes (above the device's opt-in limit: the two-pass kernel).
+size_t warp_stage_bytes(int64_t row_bytes, int dtype);
+int launch_warp(const Params& p, int dtype, int grid, size_t smem_bytes, bool staged, bool pdl,
                 void* stream);
 // Shared memory of the rows kernel for a stage size and ring depth.
 size_t rows_smem_bytes(size_t stage_bytes, int stages);

@@ -35,6 +35,10 @@ __device__ __forceinline__ void token_x(const Params& p, int64_t row_off, int64_
 #pragma unroll
         for (int e = 0; e < E; ++e) x[u][e] = 0.f;
 
+    // Whole steps (every lane's kLaneVecs vectors inside the row, the usual
+    // case) skip the per-vector bounds checks; the byte offset is formed once.
+    const bool whole = idx0 + (kLaneVecs - 1) * 32 < nvec;
+    const int64_t off = row_off + idx0 * 16;
     for (int r0 = 0; r0 < p.n_parts; r0 += kPartGroup) {
         // Every load of the group -- and, with the last group, the residual's
         // -- is issued before any is used: one memory round trip per group.
@@ -42,43 +46,32 @@ __device__ __forceinline__ void token_x(const Params& p, int64_t row_off, int64_
         uint4 raw[kPartGroup][kLaneVecs];
         uint4 res[kLaneVecs];
 #pragma unroll
-        for (int q = 0; q < kPartGroup; ++q)
+        for (int q = 0; q < kPartGroup; ++q) {
+            const int r = r0 + q < p.n_parts ? r0 + q : 0;  // any valid row when unused
+            const char* src = static_cast<const char*>(p.partials[r]) + off;
 #pragma unroll
-            for (int u = 0; u < kLaneVecs; ++u) {
-                const int64_t idx = idx0 + u * 32;
-                raw[q][u] = (r0 + q < p.n_parts && idx < nvec)
-                                ? ld_global_nc(static_cast<const char*>(p.partials[r0 + q]) +
-                                               row_off + idx * 16)
+            for (int u = 0; u < kLaneVecs; ++u)
+                raw[q][u] = (r0 + q < p.n_parts && (whole || idx0 + u * 32 < nvec))
+                                ? ld_global_nc(src + u * 32 * 16)
                                 : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-        for (int u = 0; u < kLaneVecs; ++u) {
-            const int64_t idx = idx0 + u * 32;
-            res[u] = (last && idx < nvec)
-                         ? ld_global(static_cast<const char*>(p.residual) + row_off + idx * 16)
-                         : make_uint4(0, 0, 0, 0);
         }
+#pragma unroll
+        for (int u = 0; u < kLaneVecs; ++u)
+            res[u] = (last && (whole || idx0 + u * 32 < nvec))
+                         ? ld_global(static_cast<const char*>(p.residual) + off + u * 32 * 16)
+                         : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int q = 0; q < kPartGroup; ++q) {
             if (r0 + q < p.n_parts) {
 #pragma unroll
-                for (int u = 0; u < kLaneVecs; ++u) {
-                    float f[E];
-                    V::to_float(raw[q][u], f);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) x[u][e] += f[e];
-                }
+                for (int u = 0; u < kLaneVecs; ++u)
+                    add_vec(x[u], raw[q][u], static_cast<T*>(nullptr));
             }
         }
         if (last) {
             // The residual is added after every partial, as everywhere.
 #pragma unroll
-            for (int u = 0; u < kLaneVecs; ++u) {
-                float f[E];
-                V::to_float(res[u], f);
-#pragma unroll
-                for (int e = 0; e < E; ++e) x[u][e] += f[e];
-            }
+            for (int u = 0; u < kLaneVecs; ++u) add_vec(x[u], res[u], static_cast<T*>(nullptr));
         }
     }
 }
@@ -173,7 +166,19 @@ __global__ void __launch_bounds__(kWarpTokensPerCta * 32)
                     float w[E], y[E];
                     V::to_float(ld_global_nc(static_cast<const char*>(p.weight) + idx * 16), w);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) y[e] = (x[u][e] * inv) * w[e];
+                    for (int e = 0; e < E; e += 2) {
+                        // (x * inv) * w two lanes at a time, each rounded as the
+                        // scalar multiplies are.
+                        asm("{\n\t.reg .b64 a, b, c;\n\t"
+                            "mov.b64 a, {%2, %3};\n\t"
+                            "mov.b64 b, {%4, %4};\n\t"
+                            "mul.rn.f32x2 a, a, b;\n\t"
+                            "mov.b64 c, {%5, %6};\n\t"
+                            "mul.rn.f32x2 a, a, c;\n\t"
+                            "mov.b64 {%0, %1}, a;\n\t}"
+                            : "=f"(y[e]), "=f"(y[e + 1])
+                            : "f"(x[u][e]), "f"(x[u][e + 1]), "f"(inv), "f"(w[e]), "f"(w[e + 1]));
+                    }
                     const uint4 packed = V::from_float(y);
                     for (int k = 0; k < p.n_out; ++k)
                         st_global_cs(static_cast<char*>(p.out[k]) + row_off + idx * 16, packed);

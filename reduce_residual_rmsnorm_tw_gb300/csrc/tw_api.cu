@@ -40,10 +40,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // Under TW_PATH_AUTO, a token range goes to the cluster kernel (one cluster
 // per token) when every one of its clusters can run at once -- at most
-// DeviceState::max_clusters clusters of the launch's size, the device's count
-// from the occupancy API (a cluster must fit in one GPC; on a GB300 with 152
-// SMs twelve 8-CTA clusters took 3.1 us, sixteen 5.6 us, the rows kernel 4.2
-// us) -- and to the rows kernel otherwise.  kClusterPathMaxTokens is the
+// DeviceState::max_clusters clusters of the launch's size and kernel
+// instantiation, the count from the occupancy API (a cluster must fit in one
+// GPC; on a GB300 with 152 SMs twelve 8-CTA clusters took 3.1 us, sixteen 5.6
+// us, the rows kernel 4.2 us) -- and to the rows kernel otherwise.  kClusterPathMaxTokens is the
 // bound used if the device cannot be asked.  The warp kernel is never faster
 // on this GPU (one warp cannot pull a 100+ KB token quickly) and runs only
 // when asked for.
@@ -65,9 +65,11 @@ struct DeviceState {
     int smem_optin = 0;
     bool cluster_ready = false;
     const char* cluster_error = "";
-    // Clusters of 1, 2, 4, 8 CTAs that run at once: [0] with every CTA alone
-    // on its SM (budgeted launches), [1] with CTAs free to share SMs.
-    int max_clusters[2][4] = {};
+    // Clusters of 1, 2, 4, 8 CTAs that run at once, per kernel instantiation:
+    // [0] with every CTA alone on its SM (budgeted launches), [1] with CTAs
+    // free to share SMs; then [log2 cluster][dtype][vectors per thread 1, 2,
+    // 4][partials held 2, 4, 8, 16].
+    int max_clusters[2][4][2][3][4] = {};
     unsigned int* status = nullptr;
     cudaEvent_t fork = nullptr;
     cudaEvent_t join = nullptr;
@@ -127,16 +129,19 @@ int device_state(DeviceState** out) {
             (void)cudaGetLastError();  // clear the (non-sticky) launch-API error
         }
         for (int shared = 0; shared < 2; ++shared)
-            for (int i = 0; d.cluster_ready && i < 4; ++i) {
-                int n = 0;
-                if (cluster_max_active(1 << i, shared ? 0 : kExclusiveSmemBytes, &n) !=
-                        cudaSuccess ||
-                    n < 1) {
-                    (void)cudaGetLastError();
-                    n = static_cast<int>(kClusterPathMaxTokens);
-                }
-                d.max_clusters[shared][i] = n;
-            }
+            for (int i = 0; d.cluster_ready && i < 4; ++i)
+                for (int dt = 0; dt < 2; ++dt)
+                    for (int v = 0; v < 3; ++v)
+                        for (int q = 0; q < 4; ++q) {
+                            int n = 0;
+                            if (cluster_max_active(1 << i, shared ? 0 : kExclusiveSmemBytes, dt,
+                                                   1 << v, 2 << q, &n) != cudaSuccess ||
+                                n < 1) {
+                                (void)cudaGetLastError();
+                                n = static_cast<int>(kClusterPathMaxTokens);
+                            }
+                            d.max_clusters[shared][i][dt][v][q] = n;
+                        }
         if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word)) !=
             cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress");
@@ -343,10 +348,18 @@ int launch_range(const Args& a, DeviceState& d, int64_t t0, int64_t t1, int path
     if (a.host_direct) path = TW_PATH_CLUSTER;
     int log2c = 0;
     while ((2 << log2c) <= cluster) ++log2c;
-    // Clusters that run at once with every CTA alone on its SM, and (launches
-    // without a budget only) with CTAs sharing SMs.
-    const int64_t alone = d.cluster_ready ? d.max_clusters[0][log2c] : 0;
-    const int64_t shared = d.cluster_ready && pdl ? d.max_clusters[1][log2c] : 0;
+    // Clusters of this launch's instantiation that run at once with every CTA
+    // alone on its SM, and (launches without a budget only) with CTAs
+    // sharing SMs.
+    int64_t alone = 0, shared = 0;
+    if (cluster_ok) {
+        int v = 0, q = 0;
+        while ((2 << v) <= cluster_vectors_per_thread(p.row_bytes, cluster)) ++v;
+        while ((4 << q) <= cluster_np(p.n_parts)) ++q;
+        const int dt = a.dtype == TW_BF16 ? 0 : 1;
+        alone = d.max_clusters[0][log2c][dt][v][q];
+        shared = pdl ? d.max_clusters[1][log2c][dt][v][q] : 0;
+    }
     if (path == TW_PATH_AUTO) {
         const bool fits = pdl ? tokens <= (alone > shared ? alone : shared)
                               : tokens <= alone && tokens * cluster <= sms;

@@ -231,6 +231,13 @@ void* cluster_entry_for(int vpt, int np) {
     }
 }
 
+void* cluster_kernel_for(int dtype, int vpt, int np) {
+    return dtype == TW_BF16 ? cluster_entry_for<__nv_bfloat16>(vpt, np)
+                            : cluster_entry_for<float>(vpt, np);
+}
+
+}  // namespace
+
 // Partials held in registers per thread: the smallest of 2, 4, 8, 16 that
 // covers n_parts.
 int cluster_np(int n_parts) {
@@ -238,13 +245,6 @@ int cluster_np(int n_parts) {
     while (np < n_parts) np *= 2;
     return np;
 }
-
-void* cluster_kernel_for(int dtype, int vpt, int np) {
-    return dtype == TW_BF16 ? cluster_entry_for<__nv_bfloat16>(vpt, np)
-                            : cluster_entry_for<float>(vpt, np);
-}
-
-}  // namespace
 
 int cluster_vectors_per_thread(int64_t row_bytes, int cluster) {
     const int64_t nvec = row_bytes / 16;
@@ -270,9 +270,9 @@ int cluster_set_attributes(int smem_optin) {
     return 0;
 }
 
-int cluster_max_active(int cluster, size_t smem_bytes, int* n) {
-    // Every instantiation asks for the same resources (128 threads and the
-    // given dynamic shared memory), so one stands for all.
+int cluster_max_active(int cluster, size_t smem_bytes, int dtype, int vpt, int np, int* n) {
+    // The instantiations differ in registers (by vectors per thread and
+    // partials held), so each is asked about separately.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
     cfg.blockDim = dim3(kClusterThreads);
@@ -285,7 +285,7 @@ int cluster_max_active(int cluster, size_t smem_bytes, int* n) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return static_cast<int>(
-        cudaOccupancyMaxActiveClusters(n, cluster_kernel_for(TW_BF16, 1, 8), &cfg));
+        cudaOccupancyMaxActiveClusters(n, cluster_kernel_for(dtype, vpt, np), &cfg));
 }
 
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,

@@ -116,10 +116,13 @@ int cluster_set_attributes(int smem_optin);
 int signal_prepare();
 // Vectors per thread the cluster kernel needs (0: the row is too long).
 int cluster_vectors_per_thread(int64_t row_bytes, int cluster);
-// Clusters of `cluster` CTAs of the cluster kernel, each CTA with smem_bytes of
-// dynamic shared memory, the current device can run at once (cudaError_t as
-// int).
-int cluster_max_active(int cluster, size_t smem_bytes, int* n);
+// Clusters of `cluster` CTAs of the cluster kernel instantiation for dtype,
+// vpt vectors per thread and np partials held in registers (2, 4, 8 or 16),
+// each CTA with smem_bytes of dynamic shared memory, that the current device
+// can run at once (cudaError_t as int).
+int cluster_max_active(int cluster, size_t smem_bytes, int dtype, int vpt, int np, int* n);
+// Partials the cluster kernel holds in registers for n_parts partials.
+int cluster_np(int n_parts);
 int launch_cluster(const Params& p, int dtype, int cluster, int n_clusters, size_t smem_bytes,
                    bool pdl, void* stream);
 
